@@ -1,0 +1,417 @@
+"""Benchmark of the paged-KV decode step on GB300.
+
+One step = pa_write_kv of the step's new tokens (one per decoding sequence, plus
+the prefill chunks' tokens in the mixed workload) + pa_decode over the batch (+
+pa_prefill_chunk for the chunks), one layer.  The headline workload is the
+7B-shaped MHA decode (64 sequences, 32/32 heads, head_dim 128, fp16, contexts
+U[1024, 4096], 16-token blocks, shuffled pool 1.25x the tokens): its ~2.6 GB of
+KV per step is far larger than the 129 MB L2, so every timed step reads HBM.
+
+Printed: one JSON line (rank 0).  ``value`` = algorithmic KV bytes per step /
+device time per step (CUDA events on the launching stream, inputs resident);
+``e2e`` = the same through the C ABI with the step's inputs copied from pinned
+host memory and its output copied back inside the timed region; ``roofline`` =
+the decode call's achieved KV GB/s against the measured HBM copy bandwidth;
+``cpu_baseline`` = the CPU oracle on a bounded sample of the same workload.
+
+``--impl reference`` times the CPU oracle (the only reference this repo has)
+on the same workload and prints the same line with ``impl: reference``.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn decode KV-read GB/s (% of GB300 HBM peak); decode steps/sec"
+DEFAULT_WORKLOAD = "mha-7b"
+L2_BYTES = 129 * 2 ** 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_240_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid, self.proc = uuid, None
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.uuid:
+            cmd[1:1] = ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ------------------------------------------------------------------ device workload
+
+class DeviceStep:
+    """Everything one step needs, resident on the device."""
+
+    def __init__(self, w, torch, pa, I, seed):
+        self.w, self.torch, self.pa = w, torch, pa
+        dev = "cuda"
+        src = I.source_dtype(w)
+        tdt = {"f16": torch.float16, "bf16": torch.bfloat16}
+        self.cache = pa.PagedCache(w.num_blocks, w.num_kv_heads, w.head_dim, w.cache_dtype)
+        self.err = torch.zeros(4, dtype=torch.int32, device=dev)
+        # history = every position before the step's new tokens
+        new = w.new_slot_mapping()
+        hist = []
+        for b in range(w.num_seqs):
+            L, C = int(w.context_lens[b]), int(w.q_lens[b])
+            hist.append(w.slots(b, np.arange(0, L - C)))
+        hist = np.concatenate(hist).astype(np.int32)
+        chunk = 1 << 15
+        for i in range(0, hist.size, chunk):
+            s = torch.from_numpy(hist[i:i + chunk]).to(dev)
+            shape = (s.shape[0], w.num_kv_heads, w.head_dim)
+            k = I.device_normal(shape, src, seed, 2 * i + 1)
+            v = I.device_normal(shape, src, seed, 2 * i + 2)
+            pa.pa_write_kv(self.cache, k, v, s, self.err)
+        T = w.num_q_tokens
+        self.k_new = I.device_normal((T, w.num_kv_heads, w.head_dim), src, seed, 10 ** 7)
+        self.v_new = I.device_normal((T, w.num_kv_heads, w.head_dim), src, seed, 10 ** 7 + 1)
+        self.slots = torch.from_numpy(new).to(dev)
+        self.q = I.device_normal((T, w.num_q_heads, w.head_dim), w.q_dtype, seed, 10 ** 7 + 2)
+        self.out = torch.empty_like(self.q)
+        nd = w.num_decode
+        self.nd = nd
+        self.tables = torch.from_numpy(w.block_tables).to(dev)
+        self.lens = torch.from_numpy(w.context_lens).to(dev)
+        self.cu = torch.from_numpy(w.cu_q_lens[nd:] - w.cu_q_lens[nd]).to(dev)
+        self.max_q = int(w.q_lens[nd:].max()) if w.num_seqs > nd else 0
+        self.sm = 1.0 / float(np.sqrt(w.head_dim))
+        nbytes = pa.pa_decode_workspace_bytes(nd, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                              w.max_blocks_per_seq, w.window)
+        self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+        self.reduce_launched = nbytes > 0
+        torch.cuda.synchronize()
+        if int(self.err[0]) != 0:
+            raise RuntimeError("device flags %d while filling the cache" % int(self.err[0]))
+
+    def launches_per_step(self):
+        n = 2 + (1 if self.reduce_launched else 0)
+        return n + (1 if self.max_q else 0)
+
+    def write(self):
+        self.pa.pa_write_kv(self.cache, self.k_new, self.v_new, self.slots, self.err)
+
+    def attend(self):
+        w, nd = self.w, self.nd
+        self.pa.pa_decode(self.cache, self.out[:nd], self.q[:nd], self.tables[:nd],
+                          self.lens[:nd], self.sm, w.window, self.ws, self.err)
+        if self.max_q:
+            self.pa.pa_prefill_chunk(self.cache, self.out[nd:], self.q[nd:], self.cu, self.max_q,
+                                     self.tables[nd:], self.lens[nd:], self.sm, w.window,
+                                     self.err)
+
+
+def decode_kv_bytes(w):
+    """Algorithmic KV bytes of the decode call (the decoding sequences only)."""
+    el = 1 if w.cache_dtype == "i8" else 2
+    per_tok = 2 * w.head_dim * el + (8 if w.cache_dtype == "i8" else 0)
+    L = w.context_lens[:w.num_decode].astype(np.int64)
+    eff = np.minimum(L, w.window) if w.window > 0 else L
+    return int(eff.sum()) * per_tok * w.num_kv_heads
+
+
+def time_ours(args, w, torch, pa, I, rank, world):
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    st = DeviceStep(w, torch, pa, I, seed=args.seed + 1000 * rank)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        st.write()
+        st.attend()
+    torch.cuda.synchronize()
+    try:
+        uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for e0, e1, e2 in ev:
+        e0.record(stream)
+        st.write()
+        e1.record(stream)
+        st.attend()
+        e2.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    attn_ms = [b.elapsed_time(c) for a, b, c in ev]
+    total_ms = sum(step_ms)
+    if int(st.err[0]) != 0:
+        raise RuntimeError("device flags %d during the timed steps" % int(st.err[0]))
+
+    # end to end: the step's inputs from pinned host memory, its output back
+    host = {name: getattr(st, name).cpu().pin_memory() for name in
+            ("q", "k_new", "v_new", "slots", "tables", "lens")}
+    out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_steps = max(3, min(args.steps, 200))
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s0.record(stream)
+    for _ in range(e2e_steps):
+        for name, t in host.items():
+            getattr(st, name).copy_(t, non_blocking=True)
+        st.write()
+        st.attend()
+        out_h.copy_(st.out, non_blocking=True)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = s0.elapsed_time(s1) / e2e_steps
+    return dict(step_ms=step_ms, attn_ms=attn_ms, total_ms=total_ms, clocks=clk, e2e_ms=e2e_ms,
+                h2d=h2d, d2h=d2h, launches=st.launches_per_step() * args.steps,
+                reduce=st.reduce_launched)
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+class OracleSample:
+    """The CPU oracle as it stands (single-threaded C) on a bounded sample of the
+    workload: the first few decoding sequences, each in its own small pool.  One
+    run = the write of the sequence's new token + fp64 attention of its query,
+    on the first ``heads`` kv heads (and their GQA query heads)."""
+
+    def __init__(self, w, I, nseq):
+        import oracle
+        self.oracle, self.lib, self.w = oracle, oracle.load(), w
+        self.per_tok = 2 * w.head_dim * (1 if w.cache_dtype == "i8" else 2) + (
+            8 if w.cache_dtype == "i8" else 0)
+        self.seqs = []
+        for b in range(min(nseq, w.num_decode)):
+            L = int(w.context_lens[b])
+            nblk = -(-L // w.block_size)
+            c = oracle.Cache(w.cache_dtype, nblk, w.num_kv_heads, w.head_dim)
+            kh, vh = I.history_rows(w, [b])
+            slots = np.arange(L, dtype=np.int32)
+            oracle.write_kv(c, kh[:-1], vh[:-1], I.source_dtype(w), slots[:-1], lib=self.lib)
+            self.seqs.append(dict(L=L, nblk=nblk, cache=c, k=kh[-1:], v=vh[-1:], slot=slots[-1:],
+                                  q=I.query_rows(w, [b]), subs={}))
+        self.src = I.source_dtype(w)
+
+    def run(self, i, heads=None):
+        w, o, sq = self.w, self.oracle, self.seqs[i % len(self.seqs)]
+        heads = heads or w.num_kv_heads
+        if heads not in sq["subs"]:
+            c = sq["cache"]
+            sub = o.Cache(w.cache_dtype, sq["nblk"], heads, w.head_dim, k=c.k[:, :heads],
+                          v=c.v[:, :heads],
+                          k_scale=None if c.k_scale is None else c.k_scale[:, :heads],
+                          v_scale=None if c.v_scale is None else c.v_scale[:, :heads])
+            sq["subs"][heads] = (sub, np.ascontiguousarray(sq["k"][:, :heads]),
+                                 np.ascontiguousarray(sq["v"][:, :heads]),
+                                 np.ascontiguousarray(sq["q"][:, :heads * w.group]))
+        c, k, v, q = sq["subs"][heads]
+        table = np.full((1, w.max_blocks_per_seq), -1, np.int32)
+        table[0, :sq["nblk"]] = np.arange(sq["nblk"])
+        L = sq["L"]
+        t0 = time.perf_counter()
+        o.write_kv(c, k, v, self.src, sq["slot"], lib=self.lib)
+        o.attention(c, q, w.q_dtype, np.array([0, 1], np.int32), table,
+                    np.array([L], np.int32), window=w.window, lib=self.lib)
+        dt = time.perf_counter() - t0
+        eff = min(L, w.window) if w.window > 0 else L
+        return eff * self.per_tok * heads, dt
+
+
+def cpu_baseline(w, I, budget_s, nseq=8):
+    """Repeat runs over the sample until ``budget_s`` seconds of oracle time."""
+    smp = OracleSample(w, I, nseq)
+    nbytes, spent, runs = 0, 0.0, 0
+    while spent < budget_s:
+        b, dt = smp.run(runs)
+        nbytes, spent, runs = nbytes + b, spent + dt, runs + 1
+    return nbytes / spent, len(smp.seqs), runs, spent
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    from paged_kv_cache_240_gb300 import inputs as I
+    w = I.make_workload(args.workload, seed=args.seed)
+    cfg = {"workload": args.workload, "num_seqs": w.num_seqs, "num_decode": w.num_decode,
+           "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+           "head_dim": w.head_dim, "block_size": w.block_size, "cache_dtype": w.cache_dtype,
+           "q_dtype": w.q_dtype, "window": w.window, "num_blocks": w.num_blocks,
+           "mean_context": float(w.context_lens[:w.num_decode].mean()),
+           "kv_bytes_per_step": w.kv_bytes(),
+           "l2": "inputs larger than L2" if w.kv_bytes() > 4 * L2_BYTES else
+           "inputs smaller than L2 (not flushed)"}
+    kv_step = w.kv_bytes()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+        oracle.build()
+        smp = OracleSample(w, I, nseq=4)
+        # size each step's sample so that the whole run stays near two minutes
+        per_step_s = min(args.cpu_budget, 120.0 / max(1, args.warmup + args.steps))
+        b, dt = smp.run(0)
+        heads = max(1, min(w.num_kv_heads, int(w.num_kv_heads * per_step_s / max(dt, 1e-6))))
+        rates = []
+        for i in range(args.warmup + args.steps):
+            b, dt = smp.run(i, heads)
+            if i >= args.warmup:
+                rates.append(b / dt)
+        value = statistics.median(rates) / 1e9
+        sample = ("per step: one of %d decoding sequences (whole context), %d of %d kv heads: "
+                  "write of the new token + fp64 attention" % (len(smp.seqs), heads,
+                                                                w.num_kv_heads))
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": kv_step / (value * 1e9) * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": cfg,
+                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    from __graft_entry__ import build
+    build()
+    import paged_kv_cache_240_gb300 as pa
+    r = time_ours(args, w, torch, pa, I, rank, world)
+    total_ms = r["total_ms"]
+    if world > 1:
+        t = torch.tensor([total_ms, r["e2e_ms"]], device="cuda", dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+    else:
+        e2e_ms = r["e2e_ms"]
+    ms_per_step = total_ms / args.steps
+    value = world * kv_step / (ms_per_step * 1e-3) / 1e9
+    peaks, peak_kind = measured_peaks()
+    attn_ms = statistics.mean(r["attn_ms"])
+    dec_bytes = decode_kv_bytes(w)
+    achieved = dec_bytes / (attn_ms * 1e-3) / 1e9
+    traffic = None
+    try:
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        if tr.get("kernel_source_hash") == kernel_source_hash() and tr.get("workload") == w.name:
+            traffic = tr.get("traffic_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.cache_dtype, "data": "synthetic", "config": cfg,
+            "steps_per_s": 1e3 / ms_per_step * world,
+            "hbm_frac": value / peaks["hbm_gbs"],
+            "clocks": r["clocks"],
+            "e2e": {"value": world * kv_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": r["launches"],
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": traffic,
+                         "kernel": "pa_decode (attention + split-K reduce)",
+                         "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_kind == "measured" else "fallback 6.8 TB/s"},
+            "p10_p50_p90_step_ms": [float(np.percentile(r["step_ms"], p)) for p in (10, 50, 90)]}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, nseq, runs, spent = cpu_baseline(w, I, args.cpu_budget)
+        line["cpu_baseline"] = {
+            "value": v / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d runs over %d of %d decoding sequences (whole contexts, all heads): "
+                      "write of the new token + fp64 attention, %.1f s of CPU time"
+                      % (runs, nseq, w.num_decode, spent)}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

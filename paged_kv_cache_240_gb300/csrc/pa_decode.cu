@@ -1,0 +1,359 @@
+// pa_decode.cu -- paged decode attention with split-K over the context
+// ("PyTorch LLM Serving Engine", "Loading": online softmax while walking the
+// block table; "MicroGen", Key Features: GQA via repeat_kv, sliding window).
+//
+// Grid: x = partition + num_parts * (kv head * row_groups + row group), y = seq.
+// A CTA owns one (sequence, kv head, group of up to 16 GQA query heads,
+// partition of whole blocks).  Its four consumer warps take the partition's
+// blocks round-robin, each keeping its own online-softmax state over the same 16
+// rows; the states are merged in shared memory at the end.  A sequence whose
+// visible context fits in one partition writes its output directly; otherwise
+// each partition writes (max, normaliser, unnormalised output) to the workspace
+// and pa_reduce_kernel merges them:  M = max_p m_p,
+//   out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p   (log2-domain maxima).
+// Partition boundaries and the merge order depend only on logical positions, so
+// the result is bit-identical under any relabelling of physical blocks.
+#include <algorithm>
+
+#include "pa_attn_common.cuh"
+#include "pa_internal.h"
+
+namespace pa_dev {
+
+// Number of partitions sequence `seq` needs; also gives its visible range.
+__device__ __forceinline__ int decode_parts(const AttnParams& p, int L, int& lo, int& first,
+                                            int& last) {
+  lo = p.window > 0 ? max(0, L - p.window) : 0;
+  first = lo / kBlock;
+  last = (L - 1) / kBlock;
+  return (last - first + p.part_blocks) / p.part_blocks;
+}
+
+template <int MODE, int D, typename QT>
+__global__ void __launch_bounds__(kThreads) pa_decode_kernel(const AttnParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int b = blockIdx.y;
+  const int part = blockIdx.x % p.num_parts;
+  const int hx = blockIdx.x / p.num_parts;
+  const int kvh = hx / p.row_groups, rg = hx % p.row_groups;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows = min(kRowsPerWarp, p.group - rg * kRowsPerWarp);
+  const int h0 = kvh * p.group + rg * kRowsPerWarp;  // first query head of this CTA
+  QT* out = static_cast<QT*>(p.out);
+
+  const int L = clamp_context(p, b, threadIdx.x == 0 && blockIdx.x == 0);
+  if (L == 0) {  // nothing visible: zeros
+    if (part == 0)
+      for (int idx = threadIdx.x; idx < rows * D; idx += kThreads)
+        out[((long long)b * p.num_q_heads + h0 + idx / D) * D + idx % D] = to_out<QT>(0.0f);
+    return;
+  }
+  int lo, first, last;
+  const int nparts = decode_parts(p, L, lo, first, last);
+  if (part >= nparts) return;
+  const int blk0 = first + part * p.part_blocks;
+  const int nblk = min(p.part_blocks, last + 1 - blk0);
+
+  const SmemPtrs s = smem_ptrs<MODE, D>(smem);
+  init_barriers(s, 1);
+  const int32_t* table = p.block_tables + (long long)b * p.max_blocks_per_seq + blk0;
+
+  if (warp == kConsumerWarps) {
+    produce<MODE, D>(p, s, table, kvh, nblk, lane);
+    return;
+  }
+
+  // ---------------- consumer warps
+  const int gid = lane >> 2, t = lane & 3;
+  const QT* q = static_cast<const QT*>(p.q);
+  const QT* qrow0 = gid < rows ? q + ((long long)b * p.num_q_heads + h0 + gid) * D : nullptr;
+  const QT* qrow1 = gid + 8 < rows ? q + ((long long)b * p.num_q_heads + h0 + gid + 8) * D : nullptr;
+  uint32_t qa[D / 16][4];
+  load_q<MODE, D, QT>(qa, qrow0, qrow1, t);
+  float o[D / 8][4];
+#pragma unroll
+  for (int nt = 0; nt < D / 8; nt++)
+#pragma unroll
+    for (int i = 0; i < 4; i++) o[nt][i] = 0.0f;
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
+  const int row_lo[2] = {lo, lo}, row_hi[2] = {L - 1, L - 1};
+
+  for (int i = warp; i < nblk; i += kConsumerWarps) {
+    const int slot = i % kStages;
+    if (!mbar_wait(&s.full[slot], (i / kStages) & 1)) {
+      if (lane == 0) {
+        set_flag(p.err, PA_FLAG_TIMEOUT);
+        *s.abort_flag = 1;
+      }
+      break;
+    }
+    if (s.valid[slot])
+      attend_block<MODE, D>(qa, o, m, l, s.stages + slot * Tile<MODE, D>::kStageBytes, lane,
+                            (blk0 + i) * kBlock, row_lo, row_hi, lo, L - 1, p.scale_log2);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.empty[slot]);
+  }
+#pragma unroll
+  for (int r = 0; r < 2; r++) {
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+  }
+  named_sync(1, kConsumerWarps * 32);  // every stage consumed: reuse them for the merge
+  if (*s.abort_flag) return;
+
+  constexpr int OS = Smem<MODE, D>::kMergeStride;
+  float* mw = reinterpret_cast<float*>(s.stages);      // [warp][16]
+  float* lw = mw + kConsumerWarps * kRowsPerWarp;      // [warp][16]
+  float* ow = lw + kConsumerWarps * kRowsPerWarp;      // [warp][16][OS]
+  if (t == 0) {
+    mw[warp * 16 + gid] = m[0];
+    mw[warp * 16 + gid + 8] = m[1];
+    lw[warp * 16 + gid] = l[0];
+    lw[warp * 16 + gid + 8] = l[1];
+  }
+#pragma unroll
+  for (int nt = 0; nt < D / 8; nt++)
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+      ow[(warp * 16 + gid + 8 * (i >> 1)) * OS + o_col<MODE, D>(nt, 2 * t + (i & 1))] = o[nt][i];
+  named_sync(1, kConsumerWarps * 32);
+
+  const bool direct = nparts == 1;
+  for (int idx = threadIdx.x; idx < rows * D; idx += kConsumerWarps * 32) {
+    const int r = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; w++) M = fmaxf(M, mw[w * 16 + r]);
+    float num = 0.0f, den = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; w++) {
+        const float e = exp2f(mw[w * 16 + r] - M);
+        num += e * ow[(w * 16 + r) * OS + d];
+        den += e * lw[w * 16 + r];
+      }
+    }
+    const long long hrow = (long long)b * p.num_q_heads + h0 + r;
+    if (direct) {
+      out[hrow * D + d] = to_out<QT>(den > 0.0f ? num / den : 0.0f);
+    } else {
+      const long long pi = hrow * p.num_parts + part;
+      p.ws_o[pi * D + d] = num;
+      if (d == 0) {
+        p.ws_m[pi] = M;
+        p.ws_l[pi] = den;
+      }
+    }
+  }
+}
+
+// One warp per (sequence, query head): merge that head's partition states.
+template <int D, typename QT>
+__global__ void __launch_bounds__(256) pa_reduce_kernel(const AttnParams p, int num_seqs) {
+  const int lane = threadIdx.x & 31;
+  const long long wid = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (wid >= (long long)num_seqs * p.num_q_heads) return;
+  const int b = (int)(wid / p.num_q_heads);
+  const int L = clamp_context(p, b, false);
+  if (L == 0) return;
+  int lo, first, last;
+  const int nparts = decode_parts(p, L, lo, first, last);
+  if (nparts <= 1) return;  // written directly by the attention kernel
+  const long long base = wid * p.num_parts;
+  float M = -INFINITY;
+  for (int q = 0; q < nparts; q++) M = fmaxf(M, p.ws_m[base + q]);
+  constexpr int E = D / 32;
+  float acc[E], den = 0.0f;
+#pragma unroll
+  for (int e = 0; e < E; e++) acc[e] = 0.0f;
+  if (M != -INFINITY) {
+    for (int q = 0; q < nparts; q++) {
+      const float mq = p.ws_m[base + q];
+      const float w = exp2f(mq - M);  // 0 for a partition with no visible key
+      den += w * p.ws_l[base + q];
+      const float* src = p.ws_o + (base + q) * D + lane * E;
+      if constexpr (E == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+        acc[2] += w * v.z;
+        acc[3] += w * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+      }
+    }
+  }
+  QT* out = static_cast<QT*>(p.out) + wid * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; e++) out[e] = to_out<QT>(den > 0.0f ? acc[e] / den : 0.0f);
+}
+
+}  // namespace pa_dev
+
+using namespace pa_dev;
+
+namespace {
+
+int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// Most blocks one sequence's visible context can touch.
+int max_blocks_touched(int max_blocks_per_seq, int window) {
+  if (window <= 0) return max_blocks_per_seq;
+  return std::min(max_blocks_per_seq, (window + 2 * kBlock - 2) / kBlock);
+}
+
+struct Split {
+  int part_blocks, num_parts;
+};
+
+// Partition size: 32 blocks (512 tokens) unless the batch is too small to give
+// every SM two CTAs, in which case halve it (down to 4 blocks).
+Split choose_split(int num_seqs, int num_kv_heads, int row_groups, int max_blocks_per_seq,
+                   int window, int partition_blocks) {
+  const int maxb = max_blocks_touched(max_blocks_per_seq, window);
+  int pb = partition_blocks;
+  if (pb <= 0) {
+    const long long units = (long long)num_seqs * num_kv_heads * row_groups;
+    long long target = 2LL * std::max(current_sm_count(), 1);
+    pb = 32;
+    while (pb > 4 && units * ((maxb + pb - 1) / pb) < target) pb /= 2;
+  }
+  Split s;
+  s.part_blocks = std::max(1, std::min(pb, maxb));
+  s.num_parts = (maxb + s.part_blocks - 1) / s.part_blocks;
+  return s;
+}
+
+size_t workspace_for(int num_seqs, int num_q_heads, int head_dim, const Split& s) {
+  if (s.num_parts <= 1) return 0;
+  const size_t n = (size_t)num_seqs * num_q_heads * s.num_parts;
+  return n * head_dim * 4 + 2 * n * 4 + 16;
+}
+
+template <int MODE, int D, typename QT>
+cudaError_t launch_decode(const AttnParams& p, int num_seqs, cudaStream_t stream) {
+  constexpr int smem = Smem<MODE, D>::kBytes;
+  auto kern = pa_decode_kernel<MODE, D, QT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)(p.num_parts * p.num_kv_heads * p.row_groups), (unsigned)num_seqs);
+  kern<<<grid, kThreads, smem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.num_parts <= 1) return e;
+  const long long warps = (long long)num_seqs * p.num_q_heads;
+  pa_reduce_kernel<D, QT><<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(p, num_seqs);
+  return cudaGetLastError();
+}
+
+template <int MODE, typename QT>
+cudaError_t launch_decode_d(const AttnParams& p, int head_dim, int num_seqs, cudaStream_t s) {
+  return head_dim == 128 ? launch_decode<MODE, 128, QT>(p, num_seqs, s)
+                         : launch_decode<MODE, 64, QT>(p, num_seqs, s);
+}
+
+}  // namespace
+
+extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                            int head_dim, int max_blocks_per_seq, int window,
+                                            int partition_blocks) {
+  if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads ||
+      (head_dim != 64 && head_dim != 128) || max_blocks_per_seq < 1 || window < 0 ||
+      partition_blocks < 0)
+    return (size_t)-1;
+  const int G = num_q_heads / num_kv_heads;
+  const int row_groups = (G + kRowsPerWarp - 1) / kRowsPerWarp;
+  const Split s = choose_split(num_seqs, num_kv_heads, row_groups, max_blocks_per_seq, window,
+                               partition_blocks);
+  return workspace_for(num_seqs, num_q_heads, head_dim, s);
+}
+
+extern "C" pa_status pa_decode_partitioned(const pa_cache* cache, void* out, const void* q,
+                                           pa_dtype q_dtype, int num_seqs, int num_q_heads,
+                                           const int32_t* block_tables, int max_blocks_per_seq,
+                                           const int32_t* context_lens, float sm_scale, int window,
+                                           int partition_blocks, void* workspace,
+                                           size_t workspace_bytes, int32_t* err_flag,
+                                           void* stream) {
+  using pa_internal::aligned16;
+  pa_status st = pa_internal::check_cache(cache);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0 || num_q_heads < 1 || num_q_heads % cache->num_kv_heads ||
+      max_blocks_per_seq < 1 || window < 0 || partition_blocks < 0 || !err_flag ||
+      !(sm_scale == sm_scale) || sm_scale > 3.0e38f || sm_scale < -3.0e38f)
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(block_tables) || !aligned16(context_lens) ||
+      !aligned16(err_flag))
+    return PA_ERR_INVALID_ARG;
+  if (cache->dtype == PA_I8) {
+    if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  } else if (q_dtype != cache->dtype) {
+    return PA_ERR_UNSUPPORTED;
+  }
+  if (num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+  if ((long long)max_blocks_per_seq * kBlock > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+
+  const int G = num_q_heads / cache->num_kv_heads;
+  const int row_groups = (G + kRowsPerWarp - 1) / kRowsPerWarp;
+  const Split sp = choose_split(num_seqs, cache->num_kv_heads, row_groups, max_blocks_per_seq,
+                                window, partition_blocks);
+  const size_t need = workspace_for(num_seqs, num_q_heads, cache->head_dim, sp);
+  if (need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need))
+    return PA_ERR_INVALID_ARG;
+  if ((long long)sp.num_parts * cache->num_kv_heads * row_groups > 0x7fffffffLL)
+    return PA_ERR_UNSUPPORTED;
+
+  AttnParams p = {};
+  p.q = q;
+  p.out = out;
+  p.k_cache = static_cast<const uint8_t*>(cache->k_cache);
+  p.v_cache = static_cast<const uint8_t*>(cache->v_cache);
+  p.k_scale = cache->k_scale;
+  p.v_scale = cache->v_scale;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.err = err_flag;
+  p.num_blocks = cache->num_blocks;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.num_q_heads = num_q_heads;
+  p.group = G;
+  p.row_groups = row_groups;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.window = window;
+  p.part_blocks = sp.part_blocks;
+  p.num_parts = sp.num_parts;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  if (need > 0) {
+    const size_t n = (size_t)num_seqs * num_q_heads * sp.num_parts;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_m = p.ws_o + n * cache->head_dim;
+    p.ws_l = p.ws_m + n;
+  }
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  const int D = cache->head_dim;
+  if (cache->dtype == PA_F16) e = launch_decode_d<kF16, __half>(p, D, num_seqs, s);
+  else if (cache->dtype == PA_BF16) e = launch_decode_d<kBF16, __nv_bfloat16>(p, D, num_seqs, s);
+  else if (q_dtype == PA_F16) e = launch_decode_d<kI8, __half>(p, D, num_seqs, s);
+  else e = launch_decode_d<kI8, __nv_bfloat16>(p, D, num_seqs, s);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" pa_status pa_decode(const pa_cache* cache, void* out, const void* q, pa_dtype q_dtype,
+                               int num_seqs, int num_q_heads, const int32_t* block_tables,
+                               int max_blocks_per_seq, const int32_t* context_lens, float sm_scale,
+                               int window, void* workspace, size_t workspace_bytes,
+                               int32_t* err_flag, void* stream) {
+  return pa_decode_partitioned(cache, out, q, q_dtype, num_seqs, num_q_heads, block_tables,
+                               max_blocks_per_seq, context_lens, sm_scale, window, 0, workspace,
+                               workspace_bytes, err_flag, stream);
+}

@@ -1,0 +1,202 @@
+// pa_device.cuh -- device building blocks for the sm_103a paged-KV kernels:
+// mbarrier waits with a time limit, bulk global->shared copies, warp-level
+// tensor-core MMA (m16n8k16) and exact int8 -> f16 conversion.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa_dev {
+
+constexpr int kBlock = 16;  // tokens per physical block (the pages' 16-token page)
+
+// A bounded wait gives up after this many SM clock cycles (about 2 s at 2 GHz)
+// and reports PA_FLAG_TIMEOUT instead of hanging.
+constexpr long long kWaitLimitCycles = 4000000000LL;
+
+enum Mode { kF16 = 0, kBF16 = 1, kI8 = 2 };
+
+template <int MODE>
+struct ModeTraits {
+  static constexpr int kElt = MODE == kI8 ? 1 : 2;
+};
+
+// One pipeline stage holds one (block, kv head) tile of K and of V.  Each row is
+// copied separately into a row slot padded by 16 bytes, so that the eight row
+// addresses of an ldmatrix phase fall in eight different 16-byte bank groups.
+template <int MODE, int D>
+struct Tile {
+  static constexpr int kRowBytes = D * ModeTraits<MODE>::kElt;
+  static constexpr int kRowStride = kRowBytes + 16;
+  static constexpr int kTileBytes = kBlock * kRowStride;
+  static constexpr int kScaleBytes = MODE == kI8 ? kBlock * 4 : 0;
+  static constexpr int kScaleOff = 2 * kTileBytes;
+  static constexpr int kStageBytes = (2 * kTileBytes + 2 * kScaleBytes + 127) / 128 * 128;
+  static constexpr uint32_t kTxBytes = 2 * kBlock * kRowBytes + 2 * kScaleBytes;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ------------------------------------------------------------------ mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for the phase with the given parity to complete; false if the time
+// limit ran out first.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+  return true;
+}
+
+// Bulk (non-tensor) copy global -> this CTA's shared memory; completion is
+// counted in bytes on `bar`.  dst, src and bytes are multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Named barrier over the first `threads` threads of the CTA (id 1; id 0 is
+// __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ------------------------------------------------------------------ tensor cores
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// D = A(16x16, row) * B(16x8, col) + D, fp32 accumulate.  BF16 selects bf16
+// operands, otherwise f16 (both operands always have the same type).
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  if constexpr (BF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) return pack_bf16(lo, hi);
+  else return pack_f16(lo, hi);
+}
+
+// ------------------------------------------------------------------ int8 -> f16
+
+// The f16 with bit pattern 0x64XX is 1024 + XX exactly, so a code c in
+// [-128, 127] turned into the byte c + 128 (flip the top bit) and placed under
+// 0x64 is 1024 + 128 + c; subtracting 1152 leaves c exactly.
+__device__ __forceinline__ uint32_t f16x2_minus_1152(uint32_t biased) {
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  __half2 h = __hsub2(*reinterpret_cast<__half2*>(&biased), bias);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Four codes (bytes 0..3 of w, already XOR-ed with 0x80808080) -> f16x2 pairs
+// (c0, c1) and (c2, c3).
+__device__ __forceinline__ void biased_i8x4_to_f16(uint32_t u, uint32_t& lo, uint32_t& hi) {
+  lo = f16x2_minus_1152(__byte_perm(u, 0x64646464u, 0x4140));
+  hi = f16x2_minus_1152(__byte_perm(u, 0x64646464u, 0x4342));
+}
+
+// Bytes k and k+1 of two words (already biased) -> f16x2 pairs
+// (a.k, b.k) and (a.k+1, b.k+1); k is 0 or 2.
+template <int K>
+__device__ __forceinline__ void biased_i8_pairs(uint32_t a, uint32_t b, uint32_t& p0,
+                                                uint32_t& p1) {
+  constexpr uint32_t sel = K == 0 ? 0x5140u : 0x7362u;
+  const uint32_t x = __byte_perm(a, b, sel);  // [a.k, b.k, a.k+1, b.k+1]
+  p0 = f16x2_minus_1152(__byte_perm(x, 0x64646464u, 0x4140));
+  p1 = f16x2_minus_1152(__byte_perm(x, 0x64646464u, 0x4342));
+}
+
+// ------------------------------------------------------------------ misc
+
+__device__ __forceinline__ void set_flag(int32_t* err, int bits) {
+  if (err) atomicOr(err, bits);
+}
+
+template <typename T>
+__device__ __forceinline__ T to_out(float x);
+template <>
+__device__ __forceinline__ __half to_out<__half>(float x) {
+  return __float2half_rn(x);
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+}  // namespace pa_dev

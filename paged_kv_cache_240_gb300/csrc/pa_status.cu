@@ -1,0 +1,17 @@
+// pa_status.cu -- status helpers of the C ABI.
+#include "pa.h"
+
+extern "C" const char* pa_status_str(pa_status status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_DEVICE_DATA: return "PA_ERR_DEVICE_DATA";
+  }
+  return "PA_ERR_UNKNOWN";
+}
+
+extern "C" pa_status pa_check_flags(int32_t flags) {
+  return flags == 0 ? PA_OK : PA_ERR_DEVICE_DATA;
+}

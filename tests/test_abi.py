@@ -1,0 +1,101 @@
+"""The C-ABI library builds, loads and exports every entry point include/pa.h
+declares; host-side argument checks reject bad calls before any launch (no GPU
+needed: these calls never reach CUDA)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import paged_kv_cache_240_gb300 as pa
+from paged_kv_cache_240_gb300 import _build
+
+HEADER = os.path.join(_build.INCLUDE, "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_matches_binding():
+    assert declared_functions() == sorted(pa.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (pa_[a-z_]+)\b", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    assert pa.pa_status_str(0) == "PA_OK"
+    assert pa.pa_status_str(4) == "PA_ERR_DEVICE_DATA"
+    assert pa.pa_check_flags(0) == 0
+    assert pa.pa_check_flags(pa.PA_FLAG_BLOCK_ID) == 4
+
+
+def _cache(**kw):
+    f = dict(num_blocks=4, block_size=16, num_kv_heads=2, head_dim=128, dtype=0,
+             k_cache=4096, v_cache=8192, k_scale=None, v_scale=None)
+    f.update(kw)
+    return pa._PaCacheStruct(**f)
+
+
+def test_write_rejects_bad_arguments(lib):
+    err = ctypes.c_void_p(16 * 99)
+    call = lambda c, **kw: lib.pa_write_kv(ctypes.byref(c), kw.get("k", 256), kw.get("v", 512),
+                                           kw.get("dt", 0), kw.get("slots", 768),
+                                           kw.get("n", 3), kw.get("err", err), None)
+    assert lib.pa_write_kv(None, 1, 1, 0, 1, 1, err, None) == pa.PA_ERR_INVALID_ARG
+    assert call(_cache(block_size=8)) == pa.PA_ERR_UNSUPPORTED
+    assert call(_cache(head_dim=96)) == pa.PA_ERR_UNSUPPORTED
+    assert call(_cache(dtype=7)) == pa.PA_ERR_UNSUPPORTED
+    assert call(_cache(k_cache=None)) == pa.PA_ERR_INVALID_ARG
+    assert call(_cache(k_cache=4100)) == pa.PA_ERR_INVALID_ARG          # misaligned
+    assert call(_cache(dtype=2)) == pa.PA_ERR_INVALID_ARG               # int8 without scales
+    assert call(_cache(), dt=1) == pa.PA_ERR_UNSUPPORTED                # bf16 into f16 cache
+    assert call(_cache(), n=-1) == pa.PA_ERR_INVALID_ARG
+    assert call(_cache(), err=None) == pa.PA_ERR_INVALID_ARG
+    assert call(_cache(), n=0) == pa.PA_OK                              # no-op, nothing launched
+
+
+def test_decode_rejects_bad_arguments(lib):
+    err = ctypes.c_void_p(16 * 99)
+
+    def call(c, **kw):
+        return lib.pa_decode(ctypes.byref(c), 256, 512, kw.get("qdt", 0), kw.get("B", 2),
+                             kw.get("Hq", 4), 768, kw.get("MB", 4), 1024, kw.get("sm", 0.1),
+                             kw.get("W", 0), None, 0, kw.get("err", err), None)
+    assert call(_cache(), Hq=3) == pa.PA_ERR_INVALID_ARG       # Hq % Hkv != 0
+    assert call(_cache(), qdt=1) == pa.PA_ERR_UNSUPPORTED      # q type != cache type
+    assert call(_cache(), MB=0) == pa.PA_ERR_INVALID_ARG
+    assert call(_cache(), W=-1) == pa.PA_ERR_INVALID_ARG
+    assert call(_cache(), sm=float("nan")) == pa.PA_ERR_INVALID_ARG
+    assert call(_cache(), B=0) == pa.PA_OK
+    assert lib.pa_decode_workspace_bytes(2, 3, 2, 128, 4, 0, 0) == ctypes.c_size_t(-1).value
+    assert lib.pa_decode_workspace_bytes(2, 4, 2, 96, 4, 0, 0) == ctypes.c_size_t(-1).value
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    err = ctypes.c_void_p(16 * 99)
+
+    def call(c, **kw):
+        return lib.pa_prefill_chunk(ctypes.byref(c), 256, 512, kw.get("qdt", 0), kw.get("T", 8),
+                                    kw.get("n", 2), kw.get("Hq", 4), 768, kw.get("mq", 4), 1024,
+                                    4, 1280, 0.1, 0, None, 0, kw.get("err", err), None)
+    assert call(_cache(), Hq=5) == pa.PA_ERR_INVALID_ARG
+    assert call(_cache(), mq=-1) == pa.PA_ERR_INVALID_ARG
+    assert call(_cache(), qdt=2) == pa.PA_ERR_UNSUPPORTED
+    assert call(_cache(), T=0) == pa.PA_OK
