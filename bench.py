@@ -111,7 +111,6 @@ class DeviceStep:
         self.w, self.torch, self.pa = w, torch, pa
         dev = "cuda"
         src = I.source_dtype(w)
-        tdt = {"f16": torch.float16, "bf16": torch.bfloat16}
         self.cache = pa.PagedCache(w.num_blocks, w.num_kv_heads, w.head_dim, w.cache_dtype)
         self.err = torch.zeros(4, dtype=torch.int32, device=dev)
         # history = every position before the step's new tokens
@@ -132,12 +131,17 @@ class DeviceStep:
         self.k_new = I.device_normal((T, w.num_kv_heads, w.head_dim), src, seed, 10 ** 7)
         self.v_new = I.device_normal((T, w.num_kv_heads, w.head_dim), src, seed, 10 ** 7 + 1)
         self.slots = torch.from_numpy(new).to(dev)
-        self.q = I.device_normal((T, w.num_q_heads, w.head_dim), w.q_dtype, seed, 10 ** 7 + 2)
-        self.out = torch.empty_like(self.q)
         nd = w.num_decode
         self.nd = nd
-        self.tables = torch.from_numpy(w.block_tables).to(dev)
-        self.lens = torch.from_numpy(w.context_lens).to(dev)
+        nq = int(w.cu_q_lens[nd])
+        q = I.device_normal((T, w.num_q_heads, w.head_dim), w.q_dtype, seed, 10 ** 7 + 2)
+        # decode and prefill parts as separate (aligned, contiguous) tensors
+        self.q_dec, self.q_pre = q[:nq].clone(), q[nq:].clone()
+        self.out_dec, self.out_pre = torch.empty_like(self.q_dec), torch.empty_like(self.q_pre)
+        self.tables_dec = torch.from_numpy(w.block_tables[:nd].copy()).to(dev)
+        self.tables_pre = torch.from_numpy(w.block_tables[nd:].copy()).to(dev)
+        self.lens_dec = torch.from_numpy(w.context_lens[:nd].copy()).to(dev)
+        self.lens_pre = torch.from_numpy(w.context_lens[nd:].copy()).to(dev)
         self.cu = torch.from_numpy(w.cu_q_lens[nd:] - w.cu_q_lens[nd]).to(dev)
         self.max_q = int(w.q_lens[nd:].max()) if w.num_seqs > nd else 0
         self.sm = 1.0 / float(np.sqrt(w.head_dim))
@@ -149,6 +153,11 @@ class DeviceStep:
         if int(self.err[0]) != 0:
             raise RuntimeError("device flags %d while filling the cache" % int(self.err[0]))
 
+    # tensors the end-to-end run copies in from the host every step / out after it
+    INPUTS = ("q_dec", "q_pre", "k_new", "v_new", "slots", "tables_dec", "tables_pre",
+              "lens_dec", "lens_pre", "cu")
+    OUTPUTS = ("out_dec", "out_pre")
+
     def launches_per_step(self):
         n = 2 + (1 if self.reduce_launched else 0)
         return n + (1 if self.max_q else 0)
@@ -157,13 +166,12 @@ class DeviceStep:
         self.pa.pa_write_kv(self.cache, self.k_new, self.v_new, self.slots, self.err)
 
     def attend(self):
-        w, nd = self.w, self.nd
-        self.pa.pa_decode(self.cache, self.out[:nd], self.q[:nd], self.tables[:nd],
-                          self.lens[:nd], self.sm, w.window, self.ws, self.err)
+        w = self.w
+        self.pa.pa_decode(self.cache, self.out_dec, self.q_dec, self.tables_dec, self.lens_dec,
+                          self.sm, w.window, self.ws, self.err)
         if self.max_q:
-            self.pa.pa_prefill_chunk(self.cache, self.out[nd:], self.q[nd:], self.cu, self.max_q,
-                                     self.tables[nd:], self.lens[nd:], self.sm, w.window,
-                                     self.err)
+            self.pa.pa_prefill_chunk(self.cache, self.out_pre, self.q_pre, self.cu, self.max_q,
+                                     self.tables_pre, self.lens_pre, self.sm, w.window, self.err)
 
 
 def decode_kv_bytes(w):
@@ -213,11 +221,11 @@ def time_ours(args, w, torch, pa, I, rank, world):
         raise RuntimeError("device flags %d during the timed steps" % int(st.err[0]))
 
     # end to end: the step's inputs from pinned host memory, its output back
-    host = {name: getattr(st, name).cpu().pin_memory() for name in
-            ("q", "k_new", "v_new", "slots", "tables", "lens")}
-    out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    host = {name: getattr(st, name).cpu().pin_memory() for name in st.INPUTS}
+    outs = {name: torch.empty(getattr(st, name).shape, dtype=getattr(st, name).dtype
+                              ).pin_memory() for name in st.OUTPUTS}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_h.numel() * out_h.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
     e2e_steps = max(3, min(args.steps, 200))
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -227,7 +235,8 @@ def time_ours(args, w, torch, pa, I, rank, world):
             getattr(st, name).copy_(t, non_blocking=True)
         st.write()
         st.attend()
-        out_h.copy_(st.out, non_blocking=True)
+        for name, t in outs.items():
+            t.copy_(getattr(st, name), non_blocking=True)
     s1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = s0.elapsed_time(s1) / e2e_steps
@@ -308,12 +317,14 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="fewer decoding sequences (small profiling captures)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     from paged_kv_cache_240_gb300 import inputs as I
-    w = I.make_workload(args.workload, seed=args.seed)
+    w = I.make_workload(args.workload, seed=args.seed, num_seqs=args.num_seqs)
     cfg = {"workload": args.workload, "num_seqs": w.num_seqs, "num_decode": w.num_decode,
            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
            "head_dim": w.head_dim, "block_size": w.block_size, "cache_dtype": w.cache_dtype,

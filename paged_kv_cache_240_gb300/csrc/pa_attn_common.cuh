@@ -2,12 +2,15 @@
 // attention kernels.
 //
 // CTA layout: warps 0..3 are consumers, warp 4 is the producer.  The producer
-// walks the sequence's block table and, for each logical block, copies the
-// (block, kv head) K and V tiles (and the int8 scales) into a ring of shared-
-// memory stages with bulk async copies that complete on a per-stage mbarrier.
-// Consumers wait on that barrier, run the block through tensor-core MMAs and an
-// online-softmax update, and release the stage.  Block ids outside the pool are
-// never copied: the stage is marked invalid and its keys are left out.
+// walks the sequence's block table (32 entries per coalesced load) and, for each
+// logical block, has one thread issue TMA tensor copies of the (block, kv head)
+// K and V tiles -- 16 rows x head_dim of the cache viewed as a 2-D tensor
+// [num_blocks*num_kv_heads*16, head_dim] -- plus bulk copies of the int8
+// scales, into a ring of shared-memory stages; the copies complete on a
+// per-stage mbarrier.  Consumers wait on that barrier, run the block through
+// tensor-core MMAs and an online-softmax update, and release the stage.  Block
+// ids outside the pool are never copied: the stage is marked invalid and its
+// keys are left out.
 //
 // Per-warp math (m16n8k16 MMA, fp32 accumulate).  A warp owns 16 query rows
 // (GQA heads of one token for decode, (token, head) pairs for prefill):
@@ -51,21 +54,25 @@ struct AttnParams {
   float scale_log2;                  // sm_scale * log2(e)
 };
 
-// Shared-memory layout of one CTA: stages, then barriers and per-stage flags.
+// Shared-memory layout of one CTA (from a base aligned to the swizzle atom):
+// stages, int8 scales, barriers and per-stage flags.  After the pipeline drains,
+// the decode kernel reuses the stage area to merge its warps' states.
 template <int MODE, int D>
 struct Smem {
   using T = Tile<MODE, D>;
   static constexpr int kMergeStride = D + 4;  // fp32 row stride of the warp-merge area
-  static constexpr int kMergeBytes =
-      kConsumerWarps * kRowsPerWarp * (kMergeStride + 2) * 4;
-  static constexpr int kDataBytes =
-      kStages * T::kStageBytes > kMergeBytes ? kStages * T::kStageBytes : kMergeBytes;
-  static constexpr int kBarOff = (kDataBytes + 127) / 128 * 128;
-  static constexpr int kBytes = kBarOff + 2 * kStages * 8 + kStages * 4 + 16;
+  static constexpr int kMergeBytes = kConsumerWarps * kRowsPerWarp * (kMergeStride + 2) * 4;
+  static constexpr int kStagesBytes = kStages * T::kStageBytes;
+  static constexpr int kDataBytes = kStagesBytes > kMergeBytes ? kStagesBytes : kMergeBytes;
+  static constexpr int kScaleOff = (kDataBytes + 127) / 128 * 128;
+  static constexpr int kBarOff = kScaleOff + kStages * T::kScaleBytes;
+  static constexpr int kUsed = kBarOff + 2 * kStages * 8 + kStages * 4 + 16;
+  static constexpr int kBytes = kUsed + T::kAlign;  // room to align the base
 };
 
 struct SmemPtrs {
   uint8_t* stages;
+  float* scales;  // [stage][K 16 | V 16]
   uint64_t* full;
   uint64_t* empty;
   int* valid;
@@ -73,10 +80,15 @@ struct SmemPtrs {
 };
 
 template <int MODE, int D>
-__device__ __forceinline__ SmemPtrs smem_ptrs(uint8_t* smem) {
+__device__ __forceinline__ SmemPtrs smem_ptrs(uint8_t* raw) {
+  using S = Smem<MODE, D>;
+  const uint32_t a = smem_u32(raw);
+  uint8_t* smem = raw + ((Tile<MODE, D>::kAlign - (a & (Tile<MODE, D>::kAlign - 1))) &
+                         (Tile<MODE, D>::kAlign - 1));
   SmemPtrs s;
   s.stages = smem;
-  s.full = reinterpret_cast<uint64_t*>(smem + Smem<MODE, D>::kBarOff);
+  s.scales = reinterpret_cast<float*>(smem + S::kScaleOff);
+  s.full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
   s.empty = s.full + kStages;
   s.valid = reinterpret_cast<int*>(s.empty + kStages);
   s.abort_flag = s.valid + kStages;
@@ -97,54 +109,60 @@ __device__ __forceinline__ void init_barriers(const SmemPtrs& s, int empty_count
 }
 
 // Producer warp: fill stages for logical blocks table[0 .. nblk-1] of kv head
-// kvh.  Lanes 0..15 copy the 16 K rows, lanes 16..31 the 16 V rows (one bulk
-// copy each, into padded row slots); int8 adds the two 64-byte scale runs.
+// kvh.  The warp loads 32 table entries at a time; lane 0 issues the copies.
 template <int MODE, int D>
-__device__ __forceinline__ void produce(const AttnParams& p, const SmemPtrs& s,
-                                        const int32_t* table, int kvh, int nblk, int lane) {
+__device__ __forceinline__ void produce(const AttnParams& p, const void* tmk, const void* tmv,
+                                        const SmemPtrs& s, const int32_t* table, int kvh,
+                                        int nblk, int lane) {
   using T = Tile<MODE, D>;
   int issued = 0;
-  for (int i = 0; i < nblk; i++) {
-    const int slot = i % kStages;
-    if (i >= kStages && !mbar_wait(&s.empty[slot], ((i / kStages) - 1) & 1)) {
-      if (lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
-      break;
-    }
-    const int phys = table[i];
-    const bool ok = phys >= 0 && phys < p.num_blocks;
-    if (lane == 0) {
-      s.valid[slot] = ok ? 1 : 0;
-      if (ok) {
-        mbar_arrive_expect_tx(&s.full[slot], T::kTxBytes);
-      } else {
-        set_flag(p.err, PA_FLAG_BLOCK_ID);
-        mbar_arrive(&s.full[slot]);
+  bool stop = false;
+  for (int base = 0; base < nblk && !stop; base += 32) {
+    const int mine = base + lane < nblk ? table[base + lane] : -1;
+    const int cnt = min(32, nblk - base);
+    for (int j = 0; j < cnt; j++) {
+      const int i = base + j;
+      const int slot = i % kStages;
+      if (i >= kStages && !mbar_wait(&s.empty[slot], ((i / kStages) - 1) & 1)) {
+        if (lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
+        stop = true;
+        break;
       }
-    }
-    __syncwarp();
-    if (ok) {
-      uint8_t* st = s.stages + slot * T::kStageBytes;
-      const long long row0 = ((long long)phys * p.num_kv_heads + kvh) * kBlock;
-      const int r = lane & 15;
-      const uint8_t* src = (lane < 16 ? p.k_cache : p.v_cache) + (row0 + r) * T::kRowBytes;
-      bulk_g2s(st + (lane < 16 ? 0 : T::kTileBytes) + r * T::kRowStride, src, T::kRowBytes,
-               &s.full[slot]);
-      if constexpr (MODE == kI8) {
-        if (r == 0) {
-          const float* ssrc = (lane < 16 ? p.k_scale : p.v_scale) + row0;
-          bulk_g2s(st + T::kScaleOff + (lane < 16 ? 0 : kBlock * 4), ssrc, kBlock * 4,
-                   &s.full[slot]);
+      const int phys = __shfl_sync(0xffffffffu, mine, j);
+      if (lane == 0) {
+        const bool ok = phys >= 0 && phys < p.num_blocks;
+        s.valid[slot] = ok ? 1 : 0;
+        if (ok) {
+          mbar_arrive_expect_tx(&s.full[slot], T::kTxBytes);
+          uint8_t* st = s.stages + slot * T::kStageBytes;
+          const int row0 = (phys * p.num_kv_heads + kvh) * kBlock;
+#pragma unroll
+          for (int h = 0; h < T::kChunks; h++) {
+            tma_load_2d(st + h * T::kBoxBytes, tmk, h * T::kChunkElems, row0, &s.full[slot]);
+            tma_load_2d(st + T::kTileBytes + h * T::kBoxBytes, tmv, h * T::kChunkElems, row0,
+                        &s.full[slot]);
+          }
+          if constexpr (MODE == kI8) {
+            float* sc = s.scales + slot * 2 * kBlock;
+            bulk_g2s(sc, p.k_scale + row0, kBlock * 4, &s.full[slot]);
+            bulk_g2s(sc + kBlock, p.v_scale + row0, kBlock * 4, &s.full[slot]);
+          }
+        } else {
+          set_flag(p.err, PA_FLAG_BLOCK_ID);
+          mbar_arrive(&s.full[slot]);
         }
       }
+      __syncwarp();
+      issued = i + 1;
     }
-    issued = i + 1;
   }
   // No copy may still be landing in shared memory when the CTA exits.
-  for (int i = issued > kStages ? issued - kStages : 0; i < issued; i++)
-    if (!mbar_wait(&s.full[i % kStages], (i / kStages) & 1)) {
-      if (lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
-      break;
-    }
+  if (lane == 0)
+    for (int i = issued > kStages ? issued - kStages : 0; i < issued; i++)
+      if (!mbar_wait(&s.full[i % kStages], (i / kStages) & 1)) {
+        set_flag(p.err, PA_FLAG_TIMEOUT);
+        break;
+      }
 }
 
 // Q rows -> A fragments.  f16/bf16 caches: k-step ks covers d = 16ks..16ks+15 in
@@ -197,17 +215,15 @@ __device__ __forceinline__ int o_col(int nt, int n) {
 template <int MODE, int D>
 __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], float (&o)[D / 8][4],
                                              float (&m)[2], float (&l)[2], const uint8_t* stage,
-                                             int lane, int pos0, const int (&row_lo)[2],
-                                             const int (&row_hi)[2], int keep_lo, int keep_hi,
-                                             float scale_log2) {
+                                             const float* scales, int lane, int pos0,
+                                             const int (&row_lo)[2], const int (&row_hi)[2],
+                                             int keep_lo, int keep_hi, float scale_log2) {
   using T = Tile<MODE, D>;
   constexpr bool BF = MODE == kBF16;
   const int t = lane & 3;
   const int mi = lane >> 3, mr = lane & 7;
   const uint32_t kbase = smem_u32(stage);
   const uint32_t vbase = kbase + T::kTileBytes;
-  const float* kscale = reinterpret_cast<const float*>(stage + T::kScaleOff);
-  const float* vscale = kscale + kBlock;
 
   // ---- S = Q K^T: two n-tiles of 8 tokens
   float s[2][4];
@@ -215,11 +231,12 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
   for (int nt = 0; nt < 2; nt++)
 #pragma unroll
     for (int i = 0; i < 4; i++) s[nt][i] = 0.0f;
+  const int krow = 8 * (mi >> 1) + mr;  // token row this lane addresses for ldmatrix
   if constexpr (MODE != kI8) {
 #pragma unroll
     for (int ks = 0; ks < D / 16; ks++) {
       uint32_t b[4];
-      ldsm_x4(b, kbase + (8 * (mi >> 1) + mr) * T::kRowStride + (16 * ks + 8 * (mi & 1)) * 2);
+      ldsm_x4(b, kbase + T::off(krow, 32 * ks + 16 * (mi & 1)));
       mma16816<BF>(s[0], qa[ks], b[0], b[1]);
       mma16816<BF>(s[1], qa[ks], b[2], b[3]);
     }
@@ -227,7 +244,7 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
 #pragma unroll
     for (int c = 0; c < D / 16; c += 2) {
       uint32_t r[4], lo, hi;
-      ldsm_x4(r, kbase + (8 * (mi >> 1) + mr) * T::kRowStride + (c + (mi & 1)) * 16);
+      ldsm_x4(r, kbase + T::off(krow, 16 * (c + (mi & 1))));
       biased_i8x4_to_f16(r[0] ^ 0x80808080u, lo, hi);
       mma16816<false>(s[0], qa[c], lo, hi);
       biased_i8x4_to_f16(r[1] ^ 0x80808080u, lo, hi);
@@ -249,7 +266,7 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
       const int r = i >> 1;
       const int pos = pos0 + tok;
       float x = s[nt][i] * scale_log2;
-      if constexpr (MODE == kI8) x *= kscale[tok];
+      if constexpr (MODE == kI8) x *= scales[tok];
       x = (pos >= row_lo[r] && pos <= row_hi[r]) ? x : -INFINITY;
       s[nt][i] = x;
       mx[r] = fmaxf(mx[r], x);
@@ -273,19 +290,23 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
       ls[i >> 1] += e;
       if constexpr (MODE == kI8) {
         const int tok = 8 * nt + 2 * t + (i & 1);
-        s[nt][i] = e > 0.0f ? e * vscale[tok] : 0.0f;  // V scale folded into P
+        s[nt][i] = e > 0.0f ? e * scales[kBlock + tok] : 0.0f;  // V scale folded into P
       } else {
         s[nt][i] = e;
       }
     }
 #pragma unroll
   for (int r = 0; r < 2; r++) l[r] = l[r] * corr[r] + ls[r];
+  // The running maximum rarely moves once a few blocks are in: skip the
+  // rescale when no row of the warp needs it.
+  if (!__all_sync(0xffffffffu, corr[0] == 1.0f && corr[1] == 1.0f)) {
 #pragma unroll
-  for (int nt = 0; nt < D / 8; nt++) {
-    o[nt][0] *= corr[0];
-    o[nt][1] *= corr[0];
-    o[nt][2] *= corr[1];
-    o[nt][3] *= corr[1];
+    for (int nt = 0; nt < D / 8; nt++) {
+      o[nt][0] *= corr[0];
+      o[nt][1] *= corr[0];
+      o[nt][2] *= corr[1];
+      o[nt][3] *= corr[1];
+    }
   }
   uint32_t pa[4];
   pa[0] = pack2<BF>(s[0][0], s[0][1]);  // row gid,   tokens 2t, 2t+1
@@ -295,40 +316,49 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
 
   // ---- O += P V
   if constexpr (MODE != kI8) {
-    uint32_t mk01 = 0xffffffffu, mk89 = 0xffffffffu;
-    if (pos0 < keep_lo || pos0 + kBlock - 1 > keep_hi) {
+    const int vrow = 8 * (mi & 1) + mr;
+    if (pos0 >= keep_lo && pos0 + kBlock - 1 <= keep_hi) {
+#pragma unroll
+      for (int n2 = 0; n2 < D / 16; n2++) {
+        uint32_t b[4];
+        ldsm_x4_t(b, vbase + T::off(vrow, 16 * (2 * n2 + (mi >> 1))));
+        mma16816<BF>(o[2 * n2], pa, b[0], b[1]);
+        mma16816<BF>(o[2 * n2 + 1], pa, b[2], b[3]);
+      }
+    } else {
       auto keep = [&](int tok) {
         const int pos = pos0 + tok;
         return pos >= keep_lo && pos <= keep_hi;
       };
-      mk01 = (keep(2 * t) ? 0x0000ffffu : 0u) | (keep(2 * t + 1) ? 0xffff0000u : 0u);
-      mk89 = (keep(2 * t + 8) ? 0x0000ffffu : 0u) | (keep(2 * t + 9) ? 0xffff0000u : 0u);
-    }
+      const uint32_t mk01 = (keep(2 * t) ? 0x0000ffffu : 0u) | (keep(2 * t + 1) ? 0xffff0000u : 0u);
+      const uint32_t mk89 =
+          (keep(2 * t + 8) ? 0x0000ffffu : 0u) | (keep(2 * t + 9) ? 0xffff0000u : 0u);
 #pragma unroll
-    for (int n2 = 0; n2 < D / 16; n2++) {
-      uint32_t b[4];
-      ldsm_x4_t(b, vbase + (8 * (mi & 1) + mr) * T::kRowStride + (8 * (2 * n2 + (mi >> 1))) * 2);
-      mma16816<BF>(o[2 * n2], pa, b[0] & mk01, b[1] & mk89);
-      mma16816<BF>(o[2 * n2 + 1], pa, b[2] & mk01, b[3] & mk89);
+      for (int n2 = 0; n2 < D / 16; n2++) {
+        uint32_t b[4];
+        ldsm_x4_t(b, vbase + T::off(vrow, 16 * (2 * n2 + (mi >> 1))));
+        mma16816<BF>(o[2 * n2], pa, b[0] & mk01, b[1] & mk89);
+        mma16816<BF>(o[2 * n2 + 1], pa, b[2] & mk01, b[3] & mk89);
+      }
     }
   } else {
     // Thread (gid, t) reads bytes [W*4*gid, W*4*gid + W*4) of V rows 2t, 2t+1,
     // 2t+8, 2t+9; n-tile nt then holds column d = (D/8)*gid + nt.
     constexpr int W = D / 32;
     const int gid = lane >> 2;
-    const uint8_t* vt = stage + T::kTileBytes + gid * W * 4;
+    const uint8_t* vt = stage + T::kTileBytes;
     uint32_t R[4][W];
     const int toks[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
 #pragma unroll
     for (int j = 0; j < 4; j++) {
       if constexpr (W == 4) {
-        const uint4 v4 = *reinterpret_cast<const uint4*>(vt + toks[j] * T::kRowStride);
+        const uint4 v4 = *reinterpret_cast<const uint4*>(vt + T::off(toks[j], 16 * gid));
         R[j][0] = v4.x ^ 0x80808080u;
         R[j][1] = v4.y ^ 0x80808080u;
         R[j][2] = v4.z ^ 0x80808080u;
         R[j][3] = v4.w ^ 0x80808080u;
       } else {
-        const uint2 v2 = *reinterpret_cast<const uint2*>(vt + toks[j] * T::kRowStride);
+        const uint2 v2 = *reinterpret_cast<const uint2*>(vt + T::off(toks[j], 8 * gid));
         R[j][0] = v2.x ^ 0x80808080u;
         R[j][1] = v2.y ^ 0x80808080u;
       }

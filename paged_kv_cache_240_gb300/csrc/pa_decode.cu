@@ -30,8 +30,10 @@ __device__ __forceinline__ int decode_parts(const AttnParams& p, int L, int& lo,
 }
 
 template <int MODE, int D, typename QT>
-__global__ void __launch_bounds__(kThreads) pa_decode_kernel(const AttnParams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+__global__ void __launch_bounds__(kThreads)
+    pa_decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ __align__(128) uint8_t smem[];
   const int b = blockIdx.y;
   const int part = blockIdx.x % p.num_parts;
   const int hx = blockIdx.x / p.num_parts;
@@ -59,7 +61,7 @@ __global__ void __launch_bounds__(kThreads) pa_decode_kernel(const AttnParams p)
   const int32_t* table = p.block_tables + (long long)b * p.max_blocks_per_seq + blk0;
 
   if (warp == kConsumerWarps) {
-    produce<MODE, D>(p, s, table, kvh, nblk, lane);
+    produce<MODE, D>(p, &tmk, &tmv, s, table, kvh, nblk, lane);
     return;
   }
 
@@ -88,7 +90,8 @@ __global__ void __launch_bounds__(kThreads) pa_decode_kernel(const AttnParams p)
       break;
     }
     if (s.valid[slot])
-      attend_block<MODE, D>(qa, o, m, l, s.stages + slot * Tile<MODE, D>::kStageBytes, lane,
+      attend_block<MODE, D>(qa, o, m, l, s.stages + slot * Tile<MODE, D>::kStageBytes,
+                            s.scales + slot * 2 * kBlock, lane,
                             (blk0 + i) * kBlock, row_lo, row_hi, lo, L - 1, p.scale_log2);
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.empty[slot]);
@@ -115,7 +118,8 @@ __global__ void __launch_bounds__(kThreads) pa_decode_kernel(const AttnParams p)
   for (int nt = 0; nt < D / 8; nt++)
 #pragma unroll
     for (int i = 0; i < 4; i++)
-      ow[(warp * 16 + gid + 8 * (i >> 1)) * OS + o_col<MODE, D>(nt, 2 * t + (i & 1))] = o[nt][i];
+      if (gid + 8 * (i >> 1) < rows)
+        ow[(warp * 16 + gid + 8 * (i >> 1)) * OS + o_col<MODE, D>(nt, 2 * t + (i & 1))] = o[nt][i];
   named_sync(1, kConsumerWarps * 32);
 
   const bool direct = nparts == 1;
@@ -238,13 +242,14 @@ size_t workspace_for(int num_seqs, int num_q_heads, int head_dim, const Split& s
 }
 
 template <int MODE, int D, typename QT>
-cudaError_t launch_decode(const AttnParams& p, int num_seqs, cudaStream_t stream) {
+cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                          int num_seqs, cudaStream_t stream) {
   constexpr int smem = Smem<MODE, D>::kBytes;
   auto kern = pa_decode_kernel<MODE, D, QT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(p.num_parts * p.num_kv_heads * p.row_groups), (unsigned)num_seqs);
-  kern<<<grid, kThreads, smem, stream>>>(p);
+  kern<<<grid, kThreads, smem, stream>>>(p, tmk, tmv);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.num_parts <= 1) return e;
   const long long warps = (long long)num_seqs * p.num_q_heads;
@@ -253,9 +258,10 @@ cudaError_t launch_decode(const AttnParams& p, int num_seqs, cudaStream_t stream
 }
 
 template <int MODE, typename QT>
-cudaError_t launch_decode_d(const AttnParams& p, int head_dim, int num_seqs, cudaStream_t s) {
-  return head_dim == 128 ? launch_decode<MODE, 128, QT>(p, num_seqs, s)
-                         : launch_decode<MODE, 64, QT>(p, num_seqs, s);
+cudaError_t launch_decode_d(const AttnParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                           int head_dim, int num_seqs, cudaStream_t s) {
+  return head_dim == 128 ? launch_decode<MODE, 128, QT>(p, tmk, tmv, num_seqs, s)
+                         : launch_decode<MODE, 64, QT>(p, tmk, tmv, num_seqs, s);
 }
 
 }  // namespace
@@ -298,7 +304,7 @@ extern "C" pa_status pa_decode_partitioned(const pa_cache* cache, void* out, con
   } else if (q_dtype != cache->dtype) {
     return PA_ERR_UNSUPPORTED;
   }
-  if (num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || !pa_internal::cache_rows_fit(cache)) return PA_ERR_UNSUPPORTED;
   if ((long long)max_blocks_per_seq * kBlock > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
 
   const int G = num_q_heads / cache->num_kv_heads;
@@ -338,13 +344,17 @@ extern "C" pa_status pa_decode_partitioned(const pa_cache* cache, void* out, con
     p.ws_l = p.ws_m + n;
   }
 
+  CUtensorMap tmk, tmv;
+  if (!pa_internal::encode_cache_map(&tmk, cache, cache->k_cache) ||
+      !pa_internal::encode_cache_map(&tmv, cache, cache->v_cache))
+    return PA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   const int D = cache->head_dim;
-  if (cache->dtype == PA_F16) e = launch_decode_d<kF16, __half>(p, D, num_seqs, s);
-  else if (cache->dtype == PA_BF16) e = launch_decode_d<kBF16, __nv_bfloat16>(p, D, num_seqs, s);
-  else if (q_dtype == PA_F16) e = launch_decode_d<kI8, __half>(p, D, num_seqs, s);
-  else e = launch_decode_d<kI8, __nv_bfloat16>(p, D, num_seqs, s);
+  if (cache->dtype == PA_F16) e = launch_decode_d<kF16, __half>(p, tmk, tmv, D, num_seqs, s);
+  else if (cache->dtype == PA_BF16) e = launch_decode_d<kBF16, __nv_bfloat16>(p, tmk, tmv, D, num_seqs, s);
+  else if (q_dtype == PA_F16) e = launch_decode_d<kI8, __half>(p, tmk, tmv, D, num_seqs, s);
+  else e = launch_decode_d<kI8, __nv_bfloat16>(p, tmk, tmv, D, num_seqs, s);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

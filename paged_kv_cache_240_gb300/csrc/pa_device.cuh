@@ -24,18 +24,34 @@ struct ModeTraits {
   static constexpr int kElt = MODE == kI8 ? 1 : 2;
 };
 
-// One pipeline stage holds one (block, kv head) tile of K and of V.  Each row is
-// copied separately into a row slot padded by 16 bytes, so that the eight row
-// addresses of an ldmatrix phase fall in eight different 16-byte bank groups.
+// One pipeline stage holds one (block, kv head) tile of K and one of V, each 16
+// rows of D elements.  A tile arrives by TMA as kChunks boxes of 16 rows x
+// kChunkBytes (128 bytes, or 64 for int8 with D = 64), each box written with the
+// hardware swizzle that XORs the 16-byte chunk index of a row with bits of the
+// row index (128-byte rows: row & 7; 64-byte rows: (row >> 1) & 3).  Reading
+// eight rows at the same logical column then touches eight different bank
+// groups, so ldmatrix is conflict-free.
 template <int MODE, int D>
 struct Tile {
-  static constexpr int kRowBytes = D * ModeTraits<MODE>::kElt;
-  static constexpr int kRowStride = kRowBytes + 16;
-  static constexpr int kTileBytes = kBlock * kRowStride;
-  static constexpr int kScaleBytes = MODE == kI8 ? kBlock * 4 : 0;
-  static constexpr int kScaleOff = 2 * kTileBytes;
-  static constexpr int kStageBytes = (2 * kTileBytes + 2 * kScaleBytes + 127) / 128 * 128;
-  static constexpr uint32_t kTxBytes = 2 * kBlock * kRowBytes + 2 * kScaleBytes;
+  static constexpr int kElt = ModeTraits<MODE>::kElt;
+  static constexpr int kRowBytes = D * kElt;
+  static constexpr int kChunkBytes = kRowBytes < 128 ? kRowBytes : 128;
+  static constexpr int kChunkElems = kChunkBytes / kElt;
+  static constexpr int kChunks = kRowBytes / kChunkBytes;
+  static constexpr int kBoxBytes = kBlock * kChunkBytes;
+  static constexpr int kTileBytes = kBlock * kRowBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;  // K tile, then V tile
+  static constexpr int kScaleBytes = MODE == kI8 ? 2 * kBlock * 4 : 0;  // K, V scales
+  static constexpr uint32_t kTxBytes = 2 * kTileBytes + kScaleBytes;
+  static constexpr int kAlign = kChunkBytes == 128 ? 1024 : 512;  // swizzle atom
+
+  // Byte offset inside a tile of byte `b` of row `r` (b a multiple of 16 for
+  // ldmatrix addresses; the low 4 bits pass through).
+  static __device__ __forceinline__ uint32_t off(int r, int b) {
+    const int h = b / kChunkBytes, w = b % kChunkBytes;
+    const int key = kChunkBytes == 128 ? (r & 7) : ((r >> 1) & 3);
+    return h * kBoxBytes + r * kChunkBytes + ((((w >> 4) ^ key) << 4) | (w & 15));
+  }
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -94,6 +110,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// TMA tiled copy of the box at element coordinates (x, y) of a 2-D tensor map
+// into shared memory (dst aligned to the map's swizzle atom).  x * element size
+// is a multiple of 16 at every call site.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
 

@@ -1,6 +1,7 @@
 // pa_internal.h -- host-side argument checks shared by the entry points.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap and its enums (types only; no libcuda link)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -25,6 +26,55 @@ inline pa_status check_cache(const pa_cache* c) {
     if (!aligned16(c->k_scale) || !aligned16(c->v_scale)) return PA_ERR_INVALID_ARG;
   }
   return PA_OK;
+}
+
+// The driver's tensor-map encoder, fetched once through the runtime so the
+// library does not link libcuda directly.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// 2-D TMA map over one cache tensor seen as [num_blocks*num_kv_heads*16 rows,
+// head_dim]: boxes of 16 rows x min(128, row bytes), swizzled to match the
+// kernels' shared-memory addressing (128-byte rows: 128B swizzle; 64-byte rows:
+// 64B swizzle).
+inline bool encode_cache_map(CUtensorMap* m, const pa_cache* c, void* base) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const int elt = c->dtype == PA_I8 ? 1 : 2;
+  const int row_bytes = c->head_dim * elt;
+  const int chunk = row_bytes < 128 ? row_bytes : 128;
+  const cuuint64_t dims[2] = {(cuuint64_t)c->head_dim,
+                              (cuuint64_t)c->num_blocks * c->num_kv_heads * 16};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)(chunk / elt), 16};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt = c->dtype == PA_I8    ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : c->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapSwizzle sw = chunk == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                             : CU_TENSOR_MAP_SWIZZLE_64B;
+  return fn(m, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Rows of the 2-D view must fit the kernels' 32-bit row arithmetic.
+inline bool cache_rows_fit(const pa_cache* c) {
+  return (long long)c->num_blocks * c->num_kv_heads * 16 < 0x7fffffffLL;
 }
 
 }  // namespace pa_internal

@@ -18,8 +18,10 @@ namespace pa_dev {
 constexpr int kTileRows = kConsumerWarps * kRowsPerWarp;
 
 template <int MODE, int D, typename QT>
-__global__ void __launch_bounds__(kThreads) pa_prefill_kernel(const AttnParams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+__global__ void __launch_bounds__(kThreads)
+    pa_prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ __align__(128) uint8_t smem[];
   const int n = blockIdx.y;
   const int tile = blockIdx.x % p.q_tiles;
   const int kvh = blockIdx.x / p.q_tiles;
@@ -57,7 +59,7 @@ __global__ void __launch_bounds__(kThreads) pa_prefill_kernel(const AttnParams p
   const int32_t* table = p.block_tables + (long long)n * p.max_blocks_per_seq + first;
 
   if (warp == kConsumerWarps) {
-    produce<MODE, D>(p, s, table, kvh, nblk, lane);
+    produce<MODE, D>(p, &tmk, &tmv, s, table, kvh, nblk, lane);
     return;
   }
 
@@ -115,7 +117,8 @@ __global__ void __launch_bounds__(kThreads) pa_prefill_kernel(const AttnParams p
     }
     const int pos0 = (first + i) * kBlock;
     if (s.valid[slot] && pos0 <= whi && pos0 + kBlock - 1 >= wlo)
-      attend_block<MODE, D>(qa, o, m, l, s.stages + slot * Tile<MODE, D>::kStageBytes, lane, pos0,
+      attend_block<MODE, D>(qa, o, m, l, s.stages + slot * Tile<MODE, D>::kStageBytes,
+                            s.scales + slot * 2 * kBlock, lane, pos0,
                             row_lo, row_hi, lo_u, hi_u, p.scale_log2);
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.empty[slot]);
@@ -147,20 +150,22 @@ using namespace pa_dev;
 namespace {
 
 template <int MODE, int D, typename QT>
-cudaError_t launch_prefill(const AttnParams& p, int num_seqs, cudaStream_t stream) {
+cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                           int num_seqs, cudaStream_t stream) {
   constexpr int smem = Smem<MODE, D>::kBytes;
   auto kern = pa_prefill_kernel<MODE, D, QT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(p.q_tiles * p.num_kv_heads), (unsigned)num_seqs);
-  kern<<<grid, kThreads, smem, stream>>>(p);
+  kern<<<grid, kThreads, smem, stream>>>(p, tmk, tmv);
   return cudaGetLastError();
 }
 
 template <int MODE, typename QT>
-cudaError_t launch_prefill_d(const AttnParams& p, int head_dim, int num_seqs, cudaStream_t s) {
-  return head_dim == 128 ? launch_prefill<MODE, 128, QT>(p, num_seqs, s)
-                         : launch_prefill<MODE, 64, QT>(p, num_seqs, s);
+cudaError_t launch_prefill_d(const AttnParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                           int head_dim, int num_seqs, cudaStream_t s) {
+  return head_dim == 128 ? launch_prefill<MODE, 128, QT>(p, tmk, tmv, num_seqs, s)
+                         : launch_prefill<MODE, 64, QT>(p, tmk, tmv, num_seqs, s);
 }
 
 }  // namespace
@@ -192,7 +197,7 @@ extern "C" pa_status pa_prefill_chunk(const pa_cache* cache, void* out, const vo
   } else if (q_dtype != cache->dtype) {
     return PA_ERR_UNSUPPORTED;
   }
-  if (num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || !pa_internal::cache_rows_fit(cache)) return PA_ERR_UNSUPPORTED;
   if ((long long)max_blocks_per_seq * kBlock > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   const int G = num_q_heads / cache->num_kv_heads;
   const long long tiles = ((long long)max_q_len * G + kTileRows - 1) / kTileRows;
@@ -222,12 +227,16 @@ extern "C" pa_status pa_prefill_chunk(const pa_cache* cache, void* out, const vo
   p.q_tiles = (int)tiles;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
 
+  CUtensorMap tmk, tmv;
+  if (!pa_internal::encode_cache_map(&tmk, cache, cache->k_cache) ||
+      !pa_internal::encode_cache_map(&tmv, cache, cache->v_cache))
+    return PA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   const int D = cache->head_dim;
-  if (cache->dtype == PA_F16) e = launch_prefill_d<kF16, __half>(p, D, num_seqs, s);
-  else if (cache->dtype == PA_BF16) e = launch_prefill_d<kBF16, __nv_bfloat16>(p, D, num_seqs, s);
-  else if (q_dtype == PA_F16) e = launch_prefill_d<kI8, __half>(p, D, num_seqs, s);
-  else e = launch_prefill_d<kI8, __nv_bfloat16>(p, D, num_seqs, s);
+  if (cache->dtype == PA_F16) e = launch_prefill_d<kF16, __half>(p, tmk, tmv, D, num_seqs, s);
+  else if (cache->dtype == PA_BF16) e = launch_prefill_d<kBF16, __nv_bfloat16>(p, tmk, tmv, D, num_seqs, s);
+  else if (q_dtype == PA_F16) e = launch_prefill_d<kI8, __half>(p, tmk, tmv, D, num_seqs, s);
+  else e = launch_prefill_d<kI8, __nv_bfloat16>(p, tmk, tmv, D, num_seqs, s);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
