@@ -16,8 +16,9 @@
  * Conventions shared by every entry point
  *   - All pointers named *_cache, k, v, q, out, slot_mapping, block_tables,
  *     context_lens, cu_q_lens, workspace and err_flag are DEVICE pointers owned
- *     by the caller; the library allocates nothing and keeps no state between
- *     calls.  `pa_cache` itself is a host struct read during the call.
+ *     by the caller; the library allocates nothing and, apart from the fixed
+ *     scratch array behind pa_decode_noalloc, keeps no state between calls.
+ *     `pa_cache` itself is a host struct read during the call.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream) of the current
  *     device; all work is enqueued on it asynchronously and nothing is
  *     synchronised.  The caller makes the device current.
@@ -155,6 +156,33 @@ pa_status pa_decode_partitioned(const pa_cache *cache, void *out, const void *q,
 size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                                  int head_dim, int max_blocks_per_seq, int window,
                                  int partition_blocks);
+
+/*
+ * pa_decode_noalloc -- pa_decode for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for code that is
+ * handed only its input and output buffers, such as a plugin inside a host
+ * engine that owns all allocation, or a serving loop that must never call
+ * cudaMalloc/cudaFree because those calls can synchronise the whole device.
+ *
+ * Same arguments and result as pa_decode, without workspace: the split-K
+ * partials live in a scratch array of PA_NOALLOC_SCRATCH_BYTES compiled into the
+ * library, which every device that loads the library holds until the process
+ * exits.  The call allocates nothing.
+ *   - Returns PA_ERR_UNSUPPORTED, launching nothing, when this batch's partials
+ *     would exceed PA_NOALLOC_SCRATCH_BYTES (pa_decode_workspace_bytes with
+ *     partition_blocks = 0 gives the size); use pa_decode for such batches.
+ *   - The first call on each device looks up the scratch's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls on a device share the one scratch array and it keeps the last
+ *     call's contents (nothing in it needs to start at zero).  Calls that can
+ *     run at the same time on the GPU -- on different streams, or from host
+ *     threads with no ordering between them -- race on it: serialise them.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
+pa_status pa_decode_noalloc(const pa_cache *cache, void *out, const void *q, pa_dtype q_dtype,
+                            int num_seqs, int num_q_heads, const int32_t *block_tables,
+                            int max_blocks_per_seq, const int32_t *context_lens, float sm_scale,
+                            int window, int32_t *err_flag, void *stream);
 
 /*
  * pa_prefill_chunk -- chunked prefill: each sequence's chunk of queries attends

@@ -15,7 +15,8 @@ import os
 
 __all__ = [
     "PaError", "PagedCache", "load_library", "pa_write_kv", "pa_decode",
-    "pa_decode_partitioned", "pa_decode_workspace_bytes", "pa_prefill_chunk",
+    "pa_decode_partitioned", "pa_decode_workspace_bytes", "pa_decode_noalloc",
+    "pa_prefill_chunk",
     "pa_status_str", "pa_check_flags", "PA_FLAG_SLOT_RANGE", "PA_FLAG_BLOCK_ID",
     "PA_FLAG_CONTEXT_LEN", "PA_FLAG_Q_LEN", "PA_FLAG_TIMEOUT", "EXPORTED_SYMBOLS",
 ]
@@ -28,8 +29,9 @@ PA_FLAG_SLOT_RANGE, PA_FLAG_BLOCK_ID, PA_FLAG_CONTEXT_LEN, PA_FLAG_Q_LEN, PA_FLA
     1, 2, 4, 8, 16)
 
 EXPORTED_SYMBOLS = ("pa_write_kv", "pa_decode", "pa_decode_partitioned",
-                    "pa_decode_workspace_bytes", "pa_prefill_chunk", "pa_status_str",
-                    "pa_check_flags")
+                    "pa_decode_workspace_bytes", "pa_decode_noalloc", "pa_prefill_chunk",
+                    "pa_status_str", "pa_check_flags")
+PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class PaError(RuntimeError):
@@ -63,14 +65,15 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_write_kv.argtypes = [cp, P, P, I, P, I, P, P]
     lib.pa_decode.argtypes = [cp, P, P, I, I, I, P, I, P, F, I, P, S, P, P]
     lib.pa_decode_partitioned.argtypes = [cp, P, P, I, I, I, P, I, P, F, I, I, P, S, P, P]
+    lib.pa_decode_noalloc.argtypes = [cp, P, P, I, I, I, P, I, P, F, I, P, P]
     lib.pa_decode_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
     lib.pa_decode_workspace_bytes.restype = S
     lib.pa_prefill_chunk.argtypes = [cp, P, P, I, I, I, I, P, I, P, I, P, F, I, P, S, P, P]
     lib.pa_status_str.argtypes = [I]
     lib.pa_status_str.restype = ctypes.c_char_p
     lib.pa_check_flags.argtypes = [ctypes.c_int32]
-    for name in ("pa_write_kv", "pa_decode", "pa_decode_partitioned", "pa_prefill_chunk",
-                 "pa_check_flags"):
+    for name in ("pa_write_kv", "pa_decode", "pa_decode_partitioned", "pa_decode_noalloc",
+                 "pa_prefill_chunk", "pa_check_flags"):
         getattr(lib, name).restype = I
     if path == LIB_PATH:
         _lib = lib
@@ -215,6 +218,19 @@ def pa_decode(cache: PagedCache, out, q, block_tables, context_lens, sm_scale, w
         ctypes.byref(st), _ptr(out), _ptr(q), _dtype_code(q), int(q.shape[0]), int(q.shape[1]),
         _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), float(sm_scale),
         int(window), _ptr(workspace), nbytes, _ptr(err_flag), _stream(stream)), "pa_decode")
+
+
+def pa_decode_noalloc(cache: PagedCache, out, q, block_tables, context_lens, sm_scale, window,
+                      err_flag, stream=None):
+    """pa_decode for callers that cannot allocate device memory: the split-K
+    partials use scratch compiled into the library (PA_NOALLOC_SCRATCH_BYTES per
+    device).  Raises PaError (PA_ERR_UNSUPPORTED) when a batch needs more."""
+    _check_cuda(out, q, block_tables, context_lens, err_flag)
+    st = cache.struct()
+    _raise(load_library().pa_decode_noalloc(
+        ctypes.byref(st), _ptr(out), _ptr(q), _dtype_code(q), int(q.shape[0]), int(q.shape[1]),
+        _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), float(sm_scale),
+        int(window), _ptr(err_flag), _stream(stream)), "pa_decode_noalloc")
 
 
 def pa_prefill_chunk(cache: PagedCache, out, q, cu_q_lens, max_q_len, block_tables,

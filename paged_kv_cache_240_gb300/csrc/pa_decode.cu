@@ -14,6 +14,7 @@
 // Partition boundaries and the merge order depend only on logical positions, so
 // the result is bit-identical under any relabelling of physical blocks.
 #include <algorithm>
+#include <mutex>
 
 #include "pa_attn_common.cuh"
 #include "pa_internal.h"
@@ -366,4 +367,66 @@ extern "C" pa_status pa_decode(const pa_cache* cache, void* out, const void* q, 
   return pa_decode_partitioned(cache, out, q, q_dtype, num_seqs, num_q_heads, block_tables,
                                max_blocks_per_seq, context_lens, sm_scale, window, 0, workspace,
                                workspace_bytes, err_flag, stream);
+}
+
+// ---------------------------------------------------------------------------
+// pa_decode_noalloc: pa_decode for callers that cannot allocate device memory.
+//
+// The split-K partials go to a fixed scratch array compiled into this library
+// (PA_NOALLOC_SCRATCH_BYTES per device, held from the moment a device loads the
+// library until the process exits) instead of a workspace the caller passes.
+// Its device address is looked up once per device, on that device's first call,
+// with the device current; host code never hands the array's name itself to a
+// kernel, because on the host that name only stands in for the device symbol.
+// Nothing in the scratch has to start at zero: every partial a merge reads was
+// written earlier in the same call.  All calls on a device share the one array,
+// so calls whose kernels can overlap on the GPU (different streams, or host
+// threads without ordering between them) corrupt each other's partials.
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices];  // device address of the scratch, per device ordinal
+
+pa_status noalloc_scratch(void** addr) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return PA_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *addr = g_noalloc_addr[dev];
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_decode_noalloc(const pa_cache* cache, void* out, const void* q,
+                                       pa_dtype q_dtype, int num_seqs, int num_q_heads,
+                                       const int32_t* block_tables, int max_blocks_per_seq,
+                                       const int32_t* context_lens, float sm_scale, int window,
+                                       int32_t* err_flag, void* stream) {
+  pa_status st = pa_internal::check_cache(cache);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  const size_t need =
+      pa_decode_workspace_bytes(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim,
+                                max_blocks_per_seq, window, 0);
+  if (need == (size_t)-1) return PA_ERR_INVALID_ARG;
+  if (need > (size_t)PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if (need > 0) {
+    st = noalloc_scratch(&scratch);
+    if (st != PA_OK) return st;
+  }
+  return pa_decode_partitioned(cache, out, q, q_dtype, num_seqs, num_q_heads, block_tables,
+                               max_blocks_per_seq, context_lens, sm_scale, window, 0, scratch,
+                               need, err_flag, stream);
 }

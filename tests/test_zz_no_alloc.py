@@ -1,0 +1,64 @@
+"""pa_decode_noalloc against pa_decode, through the C ABI.
+
+pa_decode_noalloc serves callers that are handed only their input and output
+buffers and may not allocate device memory (a plugin inside an engine that owns
+every allocation, or a serving loop that must not call cudaMalloc/cudaFree
+because they can synchronise the device).  Its split-K partials live in scratch
+compiled into the library instead of a caller-provided workspace.  This file is
+collected last so that a run stopping at the first failure has already run every
+other test; it also passes on its own in a fresh process.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_240_gb300 as pa
+from paged_kv_cache_240_gb300 import _build
+from paged_kv_cache_240_gb300 import inputs as I
+from gpu_util import ATOL, RTOL, bits_to_torch, device_history, i32, new_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("mha-7b", dict(num_seqs=6, lens=("uniform", 1500, 4096))),
+    ("int8-kv", dict(num_seqs=5, lens=("uniform", 700, 3000))),
+])
+def test_noalloc_matches_pa_decode_twice(name, kw):
+    _build.build()
+    w = I.make_workload(name, seed=17, **kw)
+    cache, err = device_history(w)
+    B = w.num_decode
+    need = pa.pa_decode_workspace_bytes(B, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                        w.max_blocks_per_seq, w.window)
+    assert 0 < need <= pa.PA_NOALLOC_SCRATCH_BYTES  # the scratch really is used
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    tables, lens = i32(w.block_tables), i32(w.context_lens)
+    sm = 1.0 / np.sqrt(w.head_dim)
+    for call in range(2):  # the second call finds the first call's partials in the scratch
+        q = bits_to_torch(I.normal_bits((B, w.num_q_heads, w.head_dim), w.q_dtype, 40 + call, 7),
+                          w.q_dtype)
+        ref, got = torch.empty_like(q), torch.full_like(q, float("nan"))
+        e1, e2 = new_err(), new_err()
+        pa.pa_decode(cache, ref, q, tables, lens, sm, w.window, ws, e1)
+        pa.pa_decode_noalloc(cache, got, q, tables, lens, sm, w.window, e2)
+        torch.cuda.synchronize()
+        assert int(e1[0]) == 0 and int(e2[0]) == 0
+        r, g = ref.double().cpu().numpy(), got.double().cpu().numpy()
+        assert np.isfinite(g).all()
+        assert (np.abs(g - r) <= ATOL + RTOL * np.abs(r)).all(), (name, call)
+
+
+def test_noalloc_rejects_batches_beyond_its_scratch():
+    _build.build()
+    w = I.make_workload("int8-kv", seed=1, num_seqs=2, lens=("fixed", [16, 16]))
+    cache, _ = device_history(w)
+    B = 4096  # partials of 4096 seqs x 32 heads x 16 partitions exceed the scratch
+    assert pa.pa_decode_workspace_bytes(B, 32, 8, 128, 512, 0) > pa.PA_NOALLOC_SCRATCH_BYTES
+    q = torch.zeros((B, 32, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    tables = torch.zeros((B, 512), dtype=torch.int32, device="cuda")
+    lens = torch.ones(B, dtype=torch.int32, device="cuda")
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_decode_noalloc(cache, out, q, tables, lens, 0.1, 0, new_err())
+    assert e.value.status == pa.PA_ERR_UNSUPPORTED
