@@ -3,10 +3,10 @@
 // block table; "MicroGen", Key Features: GQA via repeat_kv, sliding window).
 //
 // Grid: x = partition + num_parts * (kv head * row_groups + row group), y = seq.
-// A CTA owns one (sequence, kv head, group of up to 16 GQA query heads,
+// A CTA owns one (sequence, kv head, group of up to 8 GQA query heads,
 // partition of whole blocks).  Its four consumer warps take the partition's
-// blocks round-robin, each keeping its own online-softmax state over the same 16
-// rows; the states are merged in shared memory at the end.  A sequence whose
+// blocks round-robin, each keeping its own online-softmax state for the same
+// heads; the states are merged in shared memory at the end.  A sequence whose
 // visible context fits in one partition writes its output directly; otherwise
 // each partition writes (max, normaliser, unnormalised output) to the workspace
 // and pa_reduce_kernel merges them:  M = max_p m_p,
@@ -21,6 +21,192 @@
 
 namespace pa_dev {
 
+// Decode MMA orientation: the 16 tokens of a block are the M dimension and up to
+// eight GQA query heads of the sequence's one query token are the N dimension:
+//   S^T = K Q^T   A = K rows (ldmatrix), B = Q^T held in registers
+//   O^T += V^T P^T   A = V^T (ldmatrix.trans), B = P^T (movmatrix of S^T's C tile)
+// so a block costs 2*D/16 m16n8k16 MMAs and the O^T accumulator is D/16 tiles.
+constexpr int kDecHeads = 8;
+
+// Q^T -> B fragments: thread (g, t) holds head g.  Same d order as the K tile
+// fragments: natural for 16-bit caches; for int8 the thread's four codes of
+// a k-step are d = 16c+4t..16c+4t+3 (slots 2t,2t+1 -> d+0,1; 2t+8,2t+9 -> d+2,3).
+template <int MODE, int D, typename QT>
+__device__ __forceinline__ void load_qt(uint32_t (&qb)[D / 16][2], const QT* row, int t) {
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ks++) {
+    uint32_t lo = 0, hi = 0;
+    if (row) {
+      if constexpr (MODE != kI8) {
+        lo = *reinterpret_cast<const uint32_t*>(row + 16 * ks + 2 * t);
+        hi = *reinterpret_cast<const uint32_t*>(row + 16 * ks + 8 + 2 * t);
+      } else {
+        const uint2 raw = *reinterpret_cast<const uint2*>(row + 16 * ks + 4 * t);
+        if constexpr (std::is_same<QT, __half>::value) {
+          lo = raw.x;
+          hi = raw.y;
+        } else {
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
+          lo = pack_f16(__bfloat162float(e[0]), __bfloat162float(e[1]));
+          hi = pack_f16(__bfloat162float(e[2]), __bfloat162float(e[3]));
+        }
+      }
+    }
+    qb[ks][0] = lo;
+    qb[ks][1] = hi;
+  }
+}
+
+// Output column d of O^T tile mt, C-fragment row r (0: g, 1: g+8) of thread g.
+template <int MODE, int D>
+__device__ __forceinline__ int ot_col(int mt, int g, int r) {
+  if constexpr (MODE == kI8) return (D / 8) * g + 2 * mt + r;
+  else return 16 * mt + 8 * r + g;
+}
+
+// One 16-token block through one warp: the thread's two heads are 2t, 2t+1.
+// Keys at positions outside [lo, hi] are masked; their V rows may hold garbage
+// (tail slots, data before the window) and are zeroed before O^T += V^T P^T.
+template <int MODE, int D>
+__device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2],
+                                                 float (&o)[D / 16][4], float (&m)[2],
+                                                 float (&l)[2], const uint8_t* stage,
+                                                 const float* scales, int lane, int pos0, int lo,
+                                                 int hi, float scale_log2) {
+  using T = Tile<MODE, D>;
+  constexpr bool BF = MODE == kBF16;
+  const int g = lane >> 2, t = lane & 3;
+  const int mi = lane >> 3, mr = lane & 7;
+  const uint32_t kbase = smem_u32(stage);
+  const uint32_t vbase = kbase + T::kTileBytes;
+
+  // ---- S^T = K Q^T, two independent accumulation chains
+  float sa[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  const int krow = 8 * (mi & 1) + mr;
+  if constexpr (MODE != kI8) {
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ks++) {
+      uint32_t a[4];
+      ldsm_x4(a, kbase + T::off(krow, 32 * ks + 16 * (mi >> 1)));
+      mma16816<BF>(ks & 1 ? sb : sa, a, qb[ks][0], qb[ks][1]);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < D / 16; c += 2) {
+      uint32_t r[4], a[4];
+      ldsm_x4(r, kbase + T::off(krow, 16 * (c + (mi >> 1))));
+      biased_i8x4_to_f16(r[0] ^ 0x80808080u, a[0], a[2]);  // tokens g,   step c
+      biased_i8x4_to_f16(r[1] ^ 0x80808080u, a[1], a[3]);  // tokens g+8, step c
+      mma16816<false>(sa, a, qb[c][0], qb[c][1]);
+      biased_i8x4_to_f16(r[2] ^ 0x80808080u, a[0], a[2]);  // step c+1
+      biased_i8x4_to_f16(r[3] ^ 0x80808080u, a[1], a[3]);
+      mma16816<false>(sb, a, qb[c + 1][0], qb[c + 1][1]);
+    }
+  }
+
+  // ---- scale, mask, online softmax over tokens (log2 domain); i: token g+8(i>>1), head 2t+(i&1)
+  float s[4], mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const int tok = g + 8 * (i >> 1);
+    const int pos = pos0 + tok;
+    float x = (sa[i] + sb[i]) * scale_log2;
+    if constexpr (MODE == kI8) x *= scales[tok];
+    x = (pos >= lo && pos <= hi) ? x : -INFINITY;
+    s[i] = x;
+    mx[i & 1] = fmaxf(mx[i & 1], x);
+  }
+  float ref[2], corr[2];
+#pragma unroll
+  for (int c = 0; c < 2; c++) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1)
+      mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], off));
+    const float mn = fmaxf(m[c], mx[c]);
+    ref[c] = mn == -INFINITY ? 0.0f : mn;
+    corr[c] = exp2f(m[c] - ref[c]);
+    m[c] = mn;
+  }
+  float p[4];
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const float e = exp2f(s[i] - ref[i & 1]);
+    l[i & 1] = (i < 2 ? l[i & 1] * corr[i & 1] : l[i & 1]) + e;
+    if constexpr (MODE == kI8) p[i] = e > 0.0f ? e * scales[kBlock + g + 8 * (i >> 1)] : 0.0f;
+    else p[i] = e;
+  }
+  if (!__all_sync(0xffffffffu, corr[0] == 1.0f && corr[1] == 1.0f)) {
+#pragma unroll
+    for (int mt = 0; mt < D / 16; mt++) {
+      o[mt][0] *= corr[0];
+      o[mt][1] *= corr[1];
+      o[mt][2] *= corr[0];
+      o[mt][3] *= corr[1];
+    }
+  }
+  // P^T as the PV B operand: C tile (token g, heads 2t, 2t+1) transposed to
+  // (head g, tokens 2t, 2t+1), once for tokens 0..7 and once for 8..15.
+  const uint32_t pb0 = movmatrix_t(pack2<BF>(p[0], p[1]));
+  const uint32_t pb1 = movmatrix_t(pack2<BF>(p[2], p[3]));
+
+  // ---- O^T += V^T P^T
+  if constexpr (MODE != kI8) {
+    uint32_t mk01 = 0xffffffffu, mk89 = 0xffffffffu;
+    if (pos0 < lo || pos0 + kBlock - 1 > hi) {
+      auto keep = [&](int tok) {
+        const int pos = pos0 + tok;
+        return pos >= lo && pos <= hi;
+      };
+      mk01 = (keep(2 * t) ? 0x0000ffffu : 0u) | (keep(2 * t + 1) ? 0xffff0000u : 0u);
+      mk89 = (keep(2 * t + 8) ? 0x0000ffffu : 0u) | (keep(2 * t + 9) ? 0xffff0000u : 0u);
+    }
+    const int vrow = 8 * (mi >> 1) + mr;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; mt++) {
+      uint32_t a[4];
+      ldsm_x4_t(a, vbase + T::off(vrow, 32 * mt + 16 * (mi & 1)));
+      a[0] &= mk01;
+      a[1] &= mk01;
+      a[2] &= mk89;
+      a[3] &= mk89;
+      mma16816<BF>(o[mt], a, pb0, pb1);
+    }
+  } else {
+    // Thread (g, t) reads bytes [W*4*g, W*4*g + W*4) of V rows 2t, 2t+1, 2t+8,
+    // 2t+9; tile mt's rows g and g+8 are columns (D/8)*g + 2mt and +1.
+    constexpr int W = D / 32;
+    const uint8_t* vt = stage + T::kTileBytes;
+    uint32_t R[4][W];
+    const int toks[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      if constexpr (W == 4) {
+        const uint4 v4 = *reinterpret_cast<const uint4*>(vt + T::off(toks[j], 16 * g));
+        R[j][0] = v4.x ^ 0x80808080u;
+        R[j][1] = v4.y ^ 0x80808080u;
+        R[j][2] = v4.z ^ 0x80808080u;
+        R[j][3] = v4.w ^ 0x80808080u;
+      } else {
+        const uint2 v2 = *reinterpret_cast<const uint2*>(vt + T::off(toks[j], 8 * g));
+        R[j][0] = v2.x ^ 0x80808080u;
+        R[j][1] = v2.y ^ 0x80808080u;
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < D / 16; mt++) {
+      uint32_t a[4];
+      if (mt & 1) {
+        biased_i8_pairs<2>(R[0][mt >> 1], R[1][mt >> 1], a[0], a[1]);
+        biased_i8_pairs<2>(R[2][mt >> 1], R[3][mt >> 1], a[2], a[3]);
+      } else {
+        biased_i8_pairs<0>(R[0][mt >> 1], R[1][mt >> 1], a[0], a[1]);
+        biased_i8_pairs<0>(R[2][mt >> 1], R[3][mt >> 1], a[2], a[3]);
+      }
+      mma16816<false>(o[mt], a, pb0, pb1);
+    }
+  }
+}
+
 // Number of partitions sequence `seq` needs; also gives its visible range.
 __device__ __forceinline__ int decode_parts(const AttnParams& p, int L, int& lo, int& first,
                                             int& last) {
@@ -30,8 +216,15 @@ __device__ __forceinline__ int decode_parts(const AttnParams& p, int L, int& lo,
   return (last - first + p.part_blocks) / p.part_blocks;
 }
 
+template <int MODE, int D>
+struct DecSmem {
+  static constexpr int kOS = D + 4;  // fp32 row stride of the warp-merge area
+  static constexpr int kMergeBytes = kConsumerWarps * kDecHeads * (kOS + 2) * 4;
+  static_assert(kMergeBytes <= Smem<MODE, D>::kDataBytes, "merge area must fit the stages");
+};
+
 template <int MODE, int D, typename QT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
     pa_decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -40,8 +233,8 @@ __global__ void __launch_bounds__(kThreads)
   const int hx = blockIdx.x / p.num_parts;
   const int kvh = hx / p.row_groups, rg = hx % p.row_groups;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rows = min(kRowsPerWarp, p.group - rg * kRowsPerWarp);
-  const int h0 = kvh * p.group + rg * kRowsPerWarp;  // first query head of this CTA
+  const int rows = min(kDecHeads, p.group - rg * kDecHeads);  // query heads of this CTA
+  const int h0 = kvh * p.group + rg * kDecHeads;              // the first of them
   QT* out = static_cast<QT*>(p.out);
 
   const int L = clamp_context(p, b, threadIdx.x == 0 && blockIdx.x == 0);
@@ -67,19 +260,17 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   // ---------------- consumer warps
-  const int gid = lane >> 2, t = lane & 3;
+  const int g = lane >> 2, t = lane & 3;
   const QT* q = static_cast<const QT*>(p.q);
-  const QT* qrow0 = gid < rows ? q + ((long long)b * p.num_q_heads + h0 + gid) * D : nullptr;
-  const QT* qrow1 = gid + 8 < rows ? q + ((long long)b * p.num_q_heads + h0 + gid + 8) * D : nullptr;
-  uint32_t qa[D / 16][4];
-  load_q<MODE, D, QT>(qa, qrow0, qrow1, t);
-  float o[D / 8][4];
+  uint32_t qb[D / 16][2];
+  load_qt<MODE, D, QT>(qb, g < rows ? q + ((long long)b * p.num_q_heads + h0 + g) * D : nullptr,
+                       t);
+  float o[D / 16][4];
 #pragma unroll
-  for (int nt = 0; nt < D / 8; nt++)
+  for (int mt = 0; mt < D / 16; mt++)
 #pragma unroll
-    for (int i = 0; i < 4; i++) o[nt][i] = 0.0f;
+    for (int i = 0; i < 4; i++) o[mt][i] = 0.0f;
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
-  const int row_lo[2] = {lo, lo}, row_hi[2] = {L - 1, L - 1};
 
   for (int i = warp; i < nblk; i += kConsumerWarps) {
     const int slot = i % kStages;
@@ -91,36 +282,37 @@ __global__ void __launch_bounds__(kThreads)
       break;
     }
     if (s.valid[slot])
-      attend_block<MODE, D>(qa, o, m, l, s.stages + slot * Tile<MODE, D>::kStageBytes,
-                            s.scales + slot * 2 * kBlock, lane,
-                            (blk0 + i) * kBlock, row_lo, row_hi, lo, L - 1, p.scale_log2);
+      attend_block_dec<MODE, D>(qb, o, m, l, s.stages + slot * Tile<MODE, D>::kStageBytes,
+                                s.scales + slot * 2 * kBlock, lane, (blk0 + i) * kBlock, lo,
+                                L - 1, p.scale_log2);
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.empty[slot]);
   }
+  // the normaliser was summed per thread over its two tokens: add up the tokens
 #pragma unroll
-  for (int r = 0; r < 2; r++) {
-    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
-    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
-  }
+  for (int c = 0; c < 2; c++)
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) l[c] += __shfl_xor_sync(0xffffffffu, l[c], off);
   named_sync(1, kConsumerWarps * 32);  // every stage consumed: reuse them for the merge
   if (*s.abort_flag) return;
 
-  constexpr int OS = Smem<MODE, D>::kMergeStride;
-  float* mw = reinterpret_cast<float*>(s.stages);      // [warp][16]
-  float* lw = mw + kConsumerWarps * kRowsPerWarp;      // [warp][16]
-  float* ow = lw + kConsumerWarps * kRowsPerWarp;      // [warp][16][OS]
-  if (t == 0) {
-    mw[warp * 16 + gid] = m[0];
-    mw[warp * 16 + gid + 8] = m[1];
-    lw[warp * 16 + gid] = l[0];
-    lw[warp * 16 + gid + 8] = l[1];
+  constexpr int OS = DecSmem<MODE, D>::kOS;
+  float* mw = reinterpret_cast<float*>(s.stages);  // [warp][head]
+  float* lw = mw + kConsumerWarps * kDecHeads;     // [warp][head]
+  float* ow = lw + kConsumerWarps * kDecHeads;     // [warp][head][OS]
+  if (g == 0) {
+    mw[warp * kDecHeads + 2 * t] = m[0];
+    mw[warp * kDecHeads + 2 * t + 1] = m[1];
+    lw[warp * kDecHeads + 2 * t] = l[0];
+    lw[warp * kDecHeads + 2 * t + 1] = l[1];
   }
 #pragma unroll
-  for (int nt = 0; nt < D / 8; nt++)
+  for (int mt = 0; mt < D / 16; mt++)
 #pragma unroll
-    for (int i = 0; i < 4; i++)
-      if (gid + 8 * (i >> 1) < rows)
-        ow[(warp * 16 + gid + 8 * (i >> 1)) * OS + o_col<MODE, D>(nt, 2 * t + (i & 1))] = o[nt][i];
+    for (int i = 0; i < 4; i++) {
+      const int h = 2 * t + (i & 1);
+      if (h < rows) ow[(warp * kDecHeads + h) * OS + ot_col<MODE, D>(mt, g, i >> 1)] = o[mt][i];
+    }
   named_sync(1, kConsumerWarps * 32);
 
   const bool direct = nparts == 1;
@@ -128,14 +320,14 @@ __global__ void __launch_bounds__(kThreads)
     const int r = idx / D, d = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; w++) M = fmaxf(M, mw[w * 16 + r]);
+    for (int w = 0; w < kConsumerWarps; w++) M = fmaxf(M, mw[w * kDecHeads + r]);
     float num = 0.0f, den = 0.0f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; w++) {
-        const float e = exp2f(mw[w * 16 + r] - M);
-        num += e * ow[(w * 16 + r) * OS + d];
-        den += e * lw[w * 16 + r];
+        const float e = exp2f(mw[w * kDecHeads + r] - M);
+        num += e * ow[(w * kDecHeads + r) * OS + d];
+        den += e * lw[w * kDecHeads + r];
       }
     }
     const long long hrow = (long long)b * p.num_q_heads + h0 + r;
@@ -275,7 +467,7 @@ extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int n
       partition_blocks < 0)
     return (size_t)-1;
   const int G = num_q_heads / num_kv_heads;
-  const int row_groups = (G + kRowsPerWarp - 1) / kRowsPerWarp;
+  const int row_groups = (G + kDecHeads - 1) / kDecHeads;
   const Split s = choose_split(num_seqs, num_kv_heads, row_groups, max_blocks_per_seq, window,
                                partition_blocks);
   return workspace_for(num_seqs, num_q_heads, head_dim, s);
@@ -309,7 +501,7 @@ extern "C" pa_status pa_decode_partitioned(const pa_cache* cache, void* out, con
   if ((long long)max_blocks_per_seq * kBlock > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
 
   const int G = num_q_heads / cache->num_kv_heads;
-  const int row_groups = (G + kRowsPerWarp - 1) / kRowsPerWarp;
+  const int row_groups = (G + kDecHeads - 1) / kDecHeads;
   const Split sp = choose_split(num_seqs, cache->num_kv_heads, row_groups, max_blocks_per_seq,
                                 window, partition_blocks);
   const size_t need = workspace_for(num_seqs, num_q_heads, cache->head_dim, sp);

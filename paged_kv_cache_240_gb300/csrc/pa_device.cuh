@@ -145,6 +145,15 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
                : "r"(addr));
 }
 
+// Transpose of an 8x8 b16 matrix held one row pair per thread (the layout
+// ldmatrix and the MMA C fragment use): thread (g, t) gives row g, columns 2t,
+// 2t+1 and receives row g, columns 2t, 2t+1 of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // D = A(16x16, row) * B(16x8, col) + D, fp32 accumulate.  BF16 selects bf16
 // operands, otherwise f16 (both operands always have the same type).
 template <bool BF16>
