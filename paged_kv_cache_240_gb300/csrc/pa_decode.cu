@@ -67,10 +67,17 @@ __device__ __forceinline__ int ot_col(int mt, int g, int r) {
 // One 16-token block through one warp: the thread's two heads are 2t, 2t+1.
 // Keys at positions outside [lo, hi] are masked; their V rows may hold garbage
 // (tail slots, data before the window) and are zeroed before O^T += V^T P^T.
+//
+// int8 caches: the MMAs see each code as the exact f16 integer code + 1152, so
+// S^T comes out high by 1152 * sum_d q[h][d] (kcorr, per head, subtracted here)
+// and O^T high by 1152 * sum_j P'[j][h], where P' = P * v_scale rounded to f16
+// as the MMA sees it; that sum is kept in lv with the same online rescaling as
+// O^T and subtracted once at the end.
 template <int MODE, int D>
 __device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2],
                                                  float (&o)[D / 16][4], float (&m)[2],
-                                                 float (&l)[2], const uint8_t* stage,
+                                                 float (&l)[2], float (&lv)[2],
+                                                 const float (&kcorr)[2], const uint8_t* stage,
                                                  const float* scales, int lane, int pos0, int lo,
                                                  int hi, float scale_log2) {
   using T = Tile<MODE, D>;
@@ -95,11 +102,11 @@ __device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2]
     for (int c = 0; c < D / 16; c += 2) {
       uint32_t r[4], a[4];
       ldsm_x4(r, kbase + T::off(krow, 16 * (c + (mi >> 1))));
-      biased_i8x4_to_f16(r[0] ^ 0x80808080u, a[0], a[2]);  // tokens g,   step c
-      biased_i8x4_to_f16(r[1] ^ 0x80808080u, a[1], a[3]);  // tokens g+8, step c
+      biased_i8x4_to_f16_plus1152(r[0] ^ 0x80808080u, a[0], a[2]);  // tokens g,   step c
+      biased_i8x4_to_f16_plus1152(r[1] ^ 0x80808080u, a[1], a[3]);  // tokens g+8, step c
       mma16816<false>(sa, a, qb[c][0], qb[c][1]);
-      biased_i8x4_to_f16(r[2] ^ 0x80808080u, a[0], a[2]);  // step c+1
-      biased_i8x4_to_f16(r[3] ^ 0x80808080u, a[1], a[3]);
+      biased_i8x4_to_f16_plus1152(r[2] ^ 0x80808080u, a[0], a[2]);  // step c+1
+      biased_i8x4_to_f16_plus1152(r[3] ^ 0x80808080u, a[1], a[3]);
       mma16816<false>(sb, a, qb[c + 1][0], qb[c + 1][1]);
     }
   }
@@ -110,8 +117,9 @@ __device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2]
   for (int i = 0; i < 4; i++) {
     const int tok = g + 8 * (i >> 1);
     const int pos = pos0 + tok;
-    float x = (sa[i] + sb[i]) * scale_log2;
-    if constexpr (MODE == kI8) x *= scales[tok];
+    float x;
+    if constexpr (MODE == kI8) x = (sa[i] + sb[i] - kcorr[i & 1]) * (scale_log2 * scales[tok]);
+    else x = (sa[i] + sb[i]) * scale_log2;
     x = (pos >= lo && pos <= hi) ? x : -INFINITY;
     s[i] = x;
     mx[i & 1] = fmaxf(mx[i & 1], x);
@@ -124,13 +132,13 @@ __device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2]
       mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], off));
     const float mn = fmaxf(m[c], mx[c]);
     ref[c] = mn == -INFINITY ? 0.0f : mn;
-    corr[c] = exp2f(m[c] - ref[c]);
+    corr[c] = fast_exp2(m[c] - ref[c]);
     m[c] = mn;
   }
   float p[4];
 #pragma unroll
   for (int i = 0; i < 4; i++) {
-    const float e = exp2f(s[i] - ref[i & 1]);
+    const float e = fast_exp2(s[i] - ref[i & 1]);
     l[i & 1] = (i < 2 ? l[i & 1] * corr[i & 1] : l[i & 1]) + e;
     if constexpr (MODE == kI8) p[i] = e > 0.0f ? e * scales[kBlock + g + 8 * (i >> 1)] : 0.0f;
     else p[i] = e;
@@ -146,8 +154,15 @@ __device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2]
   }
   // P^T as the PV B operand: C tile (token g, heads 2t, 2t+1) transposed to
   // (head g, tokens 2t, 2t+1), once for tokens 0..7 and once for 8..15.
-  const uint32_t pb0 = movmatrix_t(pack2<BF>(p[0], p[1]));
-  const uint32_t pb1 = movmatrix_t(pack2<BF>(p[2], p[3]));
+  const uint32_t pk0 = pack2<BF>(p[0], p[1]), pk1 = pack2<BF>(p[2], p[3]);
+  if constexpr (MODE == kI8) {
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&pk0));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&pk1));
+    lv[0] = lv[0] * corr[0] + (f0.x + f1.x);
+    lv[1] = lv[1] * corr[1] + (f0.y + f1.y);
+  }
+  const uint32_t pb0 = movmatrix_t(pk0);
+  const uint32_t pb1 = movmatrix_t(pk1);
 
   // ---- O^T += V^T P^T
   if constexpr (MODE != kI8) {
@@ -196,11 +211,11 @@ __device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2]
     for (int mt = 0; mt < D / 16; mt++) {
       uint32_t a[4];
       if (mt & 1) {
-        biased_i8_pairs<2>(R[0][mt >> 1], R[1][mt >> 1], a[0], a[1]);
-        biased_i8_pairs<2>(R[2][mt >> 1], R[3][mt >> 1], a[2], a[3]);
+        biased_i8_pairs_plus1152<2>(R[0][mt >> 1], R[1][mt >> 1], a[0], a[1]);
+        biased_i8_pairs_plus1152<2>(R[2][mt >> 1], R[3][mt >> 1], a[2], a[3]);
       } else {
-        biased_i8_pairs<0>(R[0][mt >> 1], R[1][mt >> 1], a[0], a[1]);
-        biased_i8_pairs<0>(R[2][mt >> 1], R[3][mt >> 1], a[2], a[3]);
+        biased_i8_pairs_plus1152<0>(R[0][mt >> 1], R[1][mt >> 1], a[0], a[1]);
+        biased_i8_pairs_plus1152<0>(R[2][mt >> 1], R[3][mt >> 1], a[2], a[3]);
       }
       mma16816<false>(o[mt], a, pb0, pb1);
     }
@@ -224,7 +239,7 @@ struct DecSmem {
 };
 
 template <int MODE, int D, typename QT>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, MODE == kI8 ? 4 : 3)
     pa_decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -270,7 +285,23 @@ __global__ void __launch_bounds__(kThreads, 3)
   for (int mt = 0; mt < D / 16; mt++)
 #pragma unroll
     for (int i = 0; i < 4; i++) o[mt][i] = 0.0f;
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f}, lv[2] = {0.0f, 0.0f};
+  float kcorr[2] = {0.0f, 0.0f};
+  if constexpr (MODE == kI8) {
+    // 1152 * sum_d q[h][d] for this thread's score columns h = 2t, 2t+1
+    float qs = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ks++)
+#pragma unroll
+      for (int j = 0; j < 2; j++) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&qb[ks][j]));
+        qs += f.x + f.y;
+      }
+    qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+    qs += __shfl_xor_sync(0xffffffffu, qs, 2);  // all of head g's row
+    kcorr[0] = 1152.0f * __shfl_sync(0xffffffffu, qs, 8 * t);
+    kcorr[1] = 1152.0f * __shfl_sync(0xffffffffu, qs, 8 * t + 4);
+  }
 
   for (int i = warp; i < nblk; i += kConsumerWarps) {
     const int slot = i % kStages;
@@ -282,17 +313,27 @@ __global__ void __launch_bounds__(kThreads, 3)
       break;
     }
     if (s.valid[slot])
-      attend_block_dec<MODE, D>(qb, o, m, l, s.stages + slot * Tile<MODE, D>::kStageBytes,
+      attend_block_dec<MODE, D>(qb, o, m, l, lv, kcorr,
+                                s.stages + slot * Tile<MODE, D>::kStageBytes,
                                 s.scales + slot * 2 * kBlock, lane, (blk0 + i) * kBlock, lo,
                                 L - 1, p.scale_log2);
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.empty[slot]);
   }
-  // the normaliser was summed per thread over its two tokens: add up the tokens
+  // the normalisers were summed per thread over its two tokens: add up the tokens
 #pragma unroll
   for (int c = 0; c < 2; c++)
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) l[c] += __shfl_xor_sync(0xffffffffu, l[c], off);
+    for (int off = 4; off < 32; off <<= 1) {
+      l[c] += __shfl_xor_sync(0xffffffffu, l[c], off);
+      if constexpr (MODE == kI8) lv[c] += __shfl_xor_sync(0xffffffffu, lv[c], off);
+    }
+  if constexpr (MODE == kI8) {  // remove the 1152 carried by every V code
+#pragma unroll
+    for (int mt = 0; mt < D / 16; mt++)
+#pragma unroll
+      for (int i = 0; i < 4; i++) o[mt][i] -= 1152.0f * lv[i & 1];
+  }
   named_sync(1, kConsumerWarps * 32);  // every stage consumed: reuse them for the merge
   if (*s.abort_flag) return;
 

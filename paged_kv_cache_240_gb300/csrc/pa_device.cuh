@@ -219,6 +219,31 @@ __device__ __forceinline__ void biased_i8_pairs(uint32_t a, uint32_t b, uint32_t
   p1 = f16x2_minus_1152(__byte_perm(x, 0x64646464u, 0x4342));
 }
 
+// The same conversions without the final subtraction: each f16 holds the code
+// plus 1152 exactly.  A dot product with such values is the true one plus 1152
+// times the sum of the other operand, which the caller subtracts once.
+__device__ __forceinline__ void biased_i8x4_to_f16_plus1152(uint32_t u, uint32_t& lo,
+                                                            uint32_t& hi) {
+  lo = __byte_perm(u, 0x64646464u, 0x4140);
+  hi = __byte_perm(u, 0x64646464u, 0x4342);
+}
+
+template <int K>
+__device__ __forceinline__ void biased_i8_pairs_plus1152(uint32_t a, uint32_t b, uint32_t& p0,
+                                                         uint32_t& p1) {
+  constexpr uint32_t sel = K == 0 ? 0x5140u : 0x7362u;
+  const uint32_t x = __byte_perm(a, b, sel);
+  p0 = __byte_perm(x, 0x64646464u, 0x4140);
+  p1 = __byte_perm(x, 0x64646464u, 0x4342);
+}
+
+// 2^x with the hardware approximation (relative error below 2^-22; -inf -> 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------------ misc
 
 __device__ __forceinline__ void set_flag(int32_t* err, int bits) {
