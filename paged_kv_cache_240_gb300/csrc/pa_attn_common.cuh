@@ -95,11 +95,12 @@ __device__ __forceinline__ SmemPtrs smem_ptrs(uint8_t* raw) {
   return s;
 }
 
-__device__ __forceinline__ void init_barriers(const SmemPtrs& s, int empty_count) {
+__device__ __forceinline__ void init_barriers(const SmemPtrs& s, int full_count,
+                                              int empty_count) {
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int i = 0; i < kStages; i++) {
-      mbar_init(&s.full[i], 1);
+      mbar_init(&s.full[i], full_count);
       mbar_init(&s.empty[i], empty_count);
     }
     *s.abort_flag = 0;
@@ -142,14 +143,23 @@ __device__ __forceinline__ void produce(const AttnParams& p, const void* tmk, co
             tma_load_2d(st + T::kTileBytes + h * T::kBoxBytes, tmv, h * T::kChunkElems, row0,
                         &s.full[slot]);
           }
-          if constexpr (MODE == kI8) {
-            float* sc = s.scales + slot * 2 * kBlock;
-            bulk_g2s(sc, p.k_scale + row0, kBlock * 4, &s.full[slot]);
-            bulk_g2s(sc + kBlock, p.v_scale + row0, kBlock * 4, &s.full[slot]);
-          }
         } else {
           set_flag(p.err, PA_FLAG_BLOCK_ID);
           mbar_arrive(&s.full[slot]);
+        }
+      }
+      if constexpr (MODE == kI8) {
+        // the two 64-byte scale runs: lanes 0-3 K, lanes 4-7 V, 16 bytes each
+        if (lane < T::kScaleLanes) {
+          if (phys >= 0 && phys < p.num_blocks) {
+            const long long row0 = ((long long)phys * p.num_kv_heads + kvh) * kBlock;
+            const float* src = (lane < 4 ? p.k_scale : p.v_scale) + row0 + 4 * (lane & 3);
+            cp_async_16(s.scales + slot * 2 * kBlock + (lane < 4 ? 0 : kBlock) + 4 * (lane & 3),
+                        src);
+            cp_async_arrive_noinc(&s.full[slot]);
+          } else {
+            mbar_arrive(&s.full[slot]);
+          }
         }
       }
       __syncwarp();

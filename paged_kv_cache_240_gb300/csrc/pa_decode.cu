@@ -231,6 +231,13 @@ __device__ __forceinline__ int decode_parts(const AttnParams& p, int L, int& lo,
   return (last - first + p.part_blocks) / p.part_blocks;
 }
 
+// Consumer warp w takes blocks w, w+4, w+8, ... and waits on stage (i % kStages)
+// for the phase parity of fill i / kStages.  A parity wait only tells the two
+// most recent phases apart, so every stage must always be read by the same warp
+// (then a warp never waits on a phase more than one ahead of the barrier):
+// the stage count must be a multiple of the consumer-warp count.
+static_assert(kStages % kConsumerWarps == 0, "each decode stage must belong to one warp");
+
 template <int MODE, int D>
 struct DecSmem {
   static constexpr int kOS = D + 4;  // fp32 row stride of the warp-merge area
@@ -266,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kI8 ? 4 : 3)
   const int nblk = min(p.part_blocks, last + 1 - blk0);
 
   const SmemPtrs s = smem_ptrs<MODE, D>(smem);
-  init_barriers(s, 1);
+  init_barriers(s, Tile<MODE, D>::kFullArrivals, 1);
   const int32_t* table = p.block_tables + (long long)b * p.max_blocks_per_seq + blk0;
 
   if (warp == kConsumerWarps) {

@@ -42,7 +42,11 @@ struct Tile {
   static constexpr int kTileBytes = kBlock * kRowBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;  // K tile, then V tile
   static constexpr int kScaleBytes = MODE == kI8 ? 2 * kBlock * 4 : 0;  // K, V scales
-  static constexpr uint32_t kTxBytes = 2 * kTileBytes + kScaleBytes;
+  static constexpr uint32_t kTxBytes = 2 * kTileBytes;  // TMA bytes per stage
+  // Arrivals that complete a stage: the producer's expect-tx arrival, plus one
+  // per lane that copies int8 scales with cp.async (4 lanes x 16 bytes each).
+  static constexpr int kScaleLanes = MODE == kI8 ? 8 : 0;
+  static constexpr int kFullArrivals = 1 + kScaleLanes;
   static constexpr int kAlign = kChunkBytes == 128 ? 1024 : 512;  // swizzle atom
 
   // Byte offset inside a tile of byte `b` of row `r` (b a multiple of 16 for
@@ -123,6 +127,19 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
       "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared through the load/store unit (not
+// the TMA unit), and an arrival on `bar` once this thread's earlier cp.async
+// copies have landed; the arrival is one of the barrier's expected arrivals.
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
 }
 
 // Named barrier over the first `threads` threads of the CTA (id 1; id 0 is

@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kThreads)
   const int nblk = hi_u >= lo_u ? hi_u / kBlock - first + 1 : 0;
 
   const SmemPtrs s = smem_ptrs<MODE, D>(smem);
-  init_barriers(s, kConsumerWarps);
+  init_barriers(s, Tile<MODE, D>::kFullArrivals, kConsumerWarps);
   const int32_t* table = p.block_tables + (long long)n * p.max_blocks_per_seq + first;
 
   if (warp == kConsumerWarps) {
