@@ -231,22 +231,64 @@ __device__ __forceinline__ int decode_parts(const AttnParams& p, int L, int& lo,
   return (last - first + p.part_blocks) / p.part_blocks;
 }
 
-// Consumer warp w takes blocks w, w+4, w+8, ... and waits on stage (i % kStages)
-// for the phase parity of fill i / kStages.  A parity wait only tells the two
-// most recent phases apart, so every stage must always be read by the same warp
-// (then a warp never waits on a phase more than one ahead of the barrier):
-// the stage count must be a multiple of the consumer-warp count.
-static_assert(kStages % kConsumerWarps == 0, "each decode stage must belong to one warp");
+// Decode CTAs have no producer warp: warp w of the four owns blocks w, w+4,
+// w+8, ... of its partition and the two stages w and w+4, which hold its next
+// two blocks.  It issues the TMA copies for a block itself, and refills a stage
+// as soon as it has finished with it, so a stage is only ever waited on, read
+// and refilled by one warp and no "stage empty" barrier is needed.
+constexpr int kDecWarps = 4;
+constexpr int kDecThreads = kDecWarps * 32;
+static_assert(kStages == 2 * kDecWarps, "two stages per decode warp");
 
 template <int MODE, int D>
 struct DecSmem {
   static constexpr int kOS = D + 4;  // fp32 row stride of the warp-merge area
-  static constexpr int kMergeBytes = kConsumerWarps * kDecHeads * (kOS + 2) * 4;
+  static constexpr int kMergeBytes = kDecWarps * kDecHeads * (kOS + 2) * 4;
   static_assert(kMergeBytes <= Smem<MODE, D>::kDataBytes, "merge area must fit the stages");
 };
 
+// Warp-level copy of one block of kv head kvh into stage `slot`: lane 0 arms
+// the stage's barrier and issues the TMA boxes; for int8, lanes 0-7 fetch the
+// two 64-byte scale runs with cp.async.  A block id outside the pool is not
+// copied: the stage is marked invalid and its barrier completes at once.
+template <int MODE, int D>
+__device__ __forceinline__ void fetch_block(const AttnParams& p, const void* tmk, const void* tmv,
+                                            const SmemPtrs& s, int slot, int phys, int kvh,
+                                            int lane) {
+  using T = Tile<MODE, D>;
+  const bool ok = phys >= 0 && phys < p.num_blocks;
+  const long long row0 = ((long long)(ok ? phys : 0) * p.num_kv_heads + kvh) * kBlock;
+  if (lane == 0) {
+    s.valid[slot] = ok ? 1 : 0;
+    if (ok) {
+      mbar_arrive_expect_tx(&s.full[slot], T::kTxBytes);
+      uint8_t* st = s.stages + slot * T::kStageBytes;
+#pragma unroll
+      for (int h = 0; h < T::kChunks; h++) {
+        tma_load_2d(st + h * T::kBoxBytes, tmk, h * T::kChunkElems, (int)row0, &s.full[slot]);
+        tma_load_2d(st + T::kTileBytes + h * T::kBoxBytes, tmv, h * T::kChunkElems, (int)row0,
+                    &s.full[slot]);
+      }
+    } else {
+      set_flag(p.err, PA_FLAG_BLOCK_ID);
+      mbar_arrive(&s.full[slot]);
+    }
+  }
+  if constexpr (MODE == kI8) {
+    if (lane < T::kScaleLanes) {
+      if (ok) {
+        const float* src = (lane < 4 ? p.k_scale : p.v_scale) + row0 + 4 * (lane & 3);
+        cp_async_16(s.scales + slot * 2 * kBlock + (lane < 4 ? 0 : kBlock) + 4 * (lane & 3), src);
+        cp_async_arrive_noinc(&s.full[slot]);
+      } else {
+        mbar_arrive(&s.full[slot]);
+      }
+    }
+  }
+}
+
 template <int MODE, int D, typename QT>
-__global__ void __launch_bounds__(kThreads, MODE == kI8 ? 4 : 3)
+__global__ void __launch_bounds__(kDecThreads, MODE == kI8 ? 5 : 3)
     pa_decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -262,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kI8 ? 4 : 3)
   const int L = clamp_context(p, b, threadIdx.x == 0 && blockIdx.x == 0);
   if (L == 0) {  // nothing visible: zeros
     if (part == 0)
-      for (int idx = threadIdx.x; idx < rows * D; idx += kThreads)
+      for (int idx = threadIdx.x; idx < rows * D; idx += kDecThreads)
         out[((long long)b * p.num_q_heads + h0 + idx / D) * D + idx % D] = to_out<QT>(0.0f);
     return;
   }
@@ -271,17 +313,19 @@ __global__ void __launch_bounds__(kThreads, MODE == kI8 ? 4 : 3)
   if (part >= nparts) return;
   const int blk0 = first + part * p.part_blocks;
   const int nblk = min(p.part_blocks, last + 1 - blk0);
+  const int nmine = nblk > warp ? (nblk - warp + kDecWarps - 1) / kDecWarps : 0;  // this warp's blocks
 
   const SmemPtrs s = smem_ptrs<MODE, D>(smem);
   init_barriers(s, Tile<MODE, D>::kFullArrivals, 1);
-  const int32_t* table = p.block_tables + (long long)b * p.max_blocks_per_seq + blk0;
+  // block ids of this warp's blocks k = 0..nmine-1 (logical block blk0 + warp + 4k)
+  const int32_t* table = p.block_tables + (long long)b * p.max_blocks_per_seq + blk0 + warp;
+  int ids = lane < nmine ? table[kDecWarps * lane] : -1;
+#pragma unroll
+  for (int k = 0; k < 2; k++)
+    if (k < nmine)
+      fetch_block<MODE, D>(p, &tmk, &tmv, s, warp + kDecWarps * k,
+                           __shfl_sync(0xffffffffu, ids, k), kvh, lane);
 
-  if (warp == kConsumerWarps) {
-    produce<MODE, D>(p, &tmk, &tmv, s, table, kvh, nblk, lane);
-    return;
-  }
-
-  // ---------------- consumer warps
   const int g = lane >> 2, t = lane & 3;
   const QT* q = static_cast<const QT*>(p.q);
   uint32_t qb[D / 16][2];
@@ -310,22 +354,31 @@ __global__ void __launch_bounds__(kThreads, MODE == kI8 ? 4 : 3)
     kcorr[1] = 1152.0f * __shfl_sync(0xffffffffu, qs, 8 * t + 4);
   }
 
-  for (int i = warp; i < nblk; i += kConsumerWarps) {
-    const int slot = i % kStages;
-    if (!mbar_wait(&s.full[slot], (i / kStages) & 1)) {
-      if (lane == 0) {
-        set_flag(p.err, PA_FLAG_TIMEOUT);
-        *s.abort_flag = 1;
-      }
+  bool timed_out = false;
+  for (int k = 0; k < nmine; k++) {
+    const int slot = warp + kDecWarps * (k & 1);
+    if (!mbar_wait(&s.full[slot], (k >> 1) & 1)) {
+      if (lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
+      timed_out = true;
       break;
     }
     if (s.valid[slot])
       attend_block_dec<MODE, D>(qb, o, m, l, lv, kcorr,
                                 s.stages + slot * Tile<MODE, D>::kStageBytes,
-                                s.scales + slot * 2 * kBlock, lane, (blk0 + i) * kBlock, lo,
-                                L - 1, p.scale_log2);
+                                s.scales + slot * 2 * kBlock, lane,
+                                (blk0 + warp + kDecWarps * k) * kBlock, lo, L - 1, p.scale_log2);
     __syncwarp();
-    if (lane == 0) mbar_arrive(&s.empty[slot]);
+    if (k + 2 < nmine) {
+      if (((k + 2) & 31) == 0)  // next 32 of this warp's block ids
+        ids = (k + 2 + lane) < nmine ? table[kDecWarps * (k + 2 + lane)] : -1;
+      fetch_block<MODE, D>(p, &tmk, &tmv, s, slot, __shfl_sync(0xffffffffu, ids, (k + 2) & 31),
+                           kvh, lane);
+    }
+  }
+  if (timed_out) {  // no copy may still be landing in shared memory when the CTA exits
+    for (int k = 0; k < nmine; k++)
+      if (!mbar_wait(&s.full[warp + kDecWarps * (k & 1)], (k >> 1) & 1)) break;
+    if (lane == 0) *s.abort_flag = 1;
   }
   // the normalisers were summed per thread over its two tokens: add up the tokens
 #pragma unroll
@@ -341,13 +394,13 @@ __global__ void __launch_bounds__(kThreads, MODE == kI8 ? 4 : 3)
 #pragma unroll
       for (int i = 0; i < 4; i++) o[mt][i] -= 1152.0f * lv[i & 1];
   }
-  named_sync(1, kConsumerWarps * 32);  // every stage consumed: reuse them for the merge
+  __syncthreads();  // every stage consumed: reuse them for the merge
   if (*s.abort_flag) return;
 
   constexpr int OS = DecSmem<MODE, D>::kOS;
   float* mw = reinterpret_cast<float*>(s.stages);  // [warp][head]
-  float* lw = mw + kConsumerWarps * kDecHeads;     // [warp][head]
-  float* ow = lw + kConsumerWarps * kDecHeads;     // [warp][head][OS]
+  float* lw = mw + kDecWarps * kDecHeads;          // [warp][head]
+  float* ow = lw + kDecWarps * kDecHeads;          // [warp][head][OS]
   if (g == 0) {
     mw[warp * kDecHeads + 2 * t] = m[0];
     mw[warp * kDecHeads + 2 * t + 1] = m[1];
@@ -361,18 +414,18 @@ __global__ void __launch_bounds__(kThreads, MODE == kI8 ? 4 : 3)
       const int h = 2 * t + (i & 1);
       if (h < rows) ow[(warp * kDecHeads + h) * OS + ot_col<MODE, D>(mt, g, i >> 1)] = o[mt][i];
     }
-  named_sync(1, kConsumerWarps * 32);
+  __syncthreads();
 
   const bool direct = nparts == 1;
-  for (int idx = threadIdx.x; idx < rows * D; idx += kConsumerWarps * 32) {
+  for (int idx = threadIdx.x; idx < rows * D; idx += kDecThreads) {
     const int r = idx / D, d = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; w++) M = fmaxf(M, mw[w * kDecHeads + r]);
+    for (int w = 0; w < kDecWarps; w++) M = fmaxf(M, mw[w * kDecHeads + r]);
     float num = 0.0f, den = 0.0f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; w++) {
+      for (int w = 0; w < kDecWarps; w++) {
         const float e = exp2f(mw[w * kDecHeads + r] - M);
         num += e * ow[(w * kDecHeads + r) * OS + d];
         den += e * lw[w * kDecHeads + r];
@@ -458,7 +511,7 @@ struct Split {
   int part_blocks, num_parts;
 };
 
-// Partition size: 32 blocks (512 tokens) unless the batch is too small to give
+// Partition size: 64 blocks (1024 tokens) unless the batch is too small to give
 // every SM two CTAs, in which case halve it (down to 4 blocks).
 Split choose_split(int num_seqs, int num_kv_heads, int row_groups, int max_blocks_per_seq,
                    int window, int partition_blocks) {
@@ -467,7 +520,7 @@ Split choose_split(int num_seqs, int num_kv_heads, int row_groups, int max_block
   if (pb <= 0) {
     const long long units = (long long)num_seqs * num_kv_heads * row_groups;
     long long target = 2LL * std::max(current_sm_count(), 1);
-    pb = 32;
+    pb = 64;
     while (pb > 4 && units * ((maxb + pb - 1) / pb) < target) pb /= 2;
   }
   Split s;
@@ -490,7 +543,7 @@ cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tmk, const CUt
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(p.num_parts * p.num_kv_heads * p.row_groups), (unsigned)num_seqs);
-  kern<<<grid, kThreads, smem, stream>>>(p, tmk, tmv);
+  kern<<<grid, kDecThreads, smem, stream>>>(p, tmk, tmv);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.num_parts <= 1) return e;
   const long long warps = (long long)num_seqs * p.num_q_heads;
