@@ -39,13 +39,26 @@ L2_BYTES = 129 * 2 ** 20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_240_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(files):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per pa_decode call from the committed ncu record, or None when
+    the decode sources changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if tr.get("kernel_source_hash") != kernel_source_hash(tr.get("kernel_sources", [])):
+        return None
+    return tr.get("traffic_bytes_per_launch", {}).get(workload)
 
 
 def measured_peaks():
@@ -165,13 +178,31 @@ class DeviceStep:
     def write(self):
         self.pa.pa_write_kv(self.cache, self.k_new, self.v_new, self.slots, self.err)
 
-    def attend(self):
-        w = self.w
+    def decode(self):
         self.pa.pa_decode(self.cache, self.out_dec, self.q_dec, self.tables_dec, self.lens_dec,
-                          self.sm, w.window, self.ws, self.err)
+                          self.sm, self.w.window, self.ws, self.err)
+
+    def prefill(self):
         if self.max_q:
             self.pa.pa_prefill_chunk(self.cache, self.out_pre, self.q_pre, self.cu, self.max_q,
-                                     self.tables_pre, self.lens_pre, self.sm, w.window, self.err)
+                                     self.tables_pre, self.lens_pre, self.sm, self.w.window,
+                                     self.err)
+
+    def attend(self):
+        self.decode()
+        self.prefill()
+
+
+def prefill_flops(w):
+    """Tensor-core work of the prefill chunks: 2*D flops for q.k and 2*D for p*v
+    per (query, head, visible key)."""
+    total = 0
+    for b in range(w.num_decode, w.num_seqs):
+        L, C = int(w.context_lens[b]), int(w.q_lens[b])
+        pos = np.arange(L - C, L, dtype=np.int64)
+        keys = np.minimum(pos + 1, w.window) if w.window > 0 else pos + 1
+        total += int(keys.sum()) * w.num_q_heads * 4 * w.head_dim
+    return total
 
 
 def decode_kv_bytes(w):
@@ -197,25 +228,27 @@ def time_ours(args, w, torch, pa, I, rank, world):
     except Exception:
         uuid = None
     clocks = ClockSampler(uuid)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    for e0, e1, e2 in ev:
+    for e0, e1, e2, e3 in ev:
         e0.record(stream)
         st.write()
         e1.record(stream)
-        st.attend()
+        st.decode()
         e2.record(stream)
+        st.prefill()
+        e3.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(c) for a, b, c in ev]
-    attn_ms = [b.elapsed_time(c) for a, b, c in ev]
+    step_ms = [a.elapsed_time(d) for a, b, c, d in ev]
+    dec_ms = [b.elapsed_time(c) for a, b, c, d in ev]
+    pre_ms = [c.elapsed_time(d) for a, b, c, d in ev] if st.max_q else [0.0]
     total_ms = sum(step_ms)
     if int(st.err[0]) != 0:
         raise RuntimeError("device flags %d during the timed steps" % int(st.err[0]))
@@ -240,7 +273,8 @@ def time_ours(args, w, torch, pa, I, rank, world):
     s1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = s0.elapsed_time(s1) / e2e_steps
-    return dict(step_ms=step_ms, attn_ms=attn_ms, total_ms=total_ms, clocks=clk, e2e_ms=e2e_ms,
+    return dict(step_ms=step_ms, dec_ms=dec_ms, pre_ms=pre_ms, total_ms=total_ms, clocks=clk,
+                e2e_ms=e2e_ms,
                 h2d=h2d, d2h=d2h, launches=st.launches_per_step() * args.steps,
                 reduce=st.reduce_launched)
 
@@ -383,17 +417,21 @@ def main():
     ms_per_step = total_ms / args.steps
     value = world * kv_step / (ms_per_step * 1e-3) / 1e9
     peaks, peak_kind = measured_peaks()
-    attn_ms = statistics.mean(r["attn_ms"])
-    dec_bytes = decode_kv_bytes(w)
-    achieved = dec_bytes / (attn_ms * 1e-3) / 1e9
-    traffic = None
-    try:
-        with open(TRAFFIC_FILE) as f:
-            tr = json.load(f)
-        if tr.get("kernel_source_hash") == kernel_source_hash() and tr.get("workload") == w.name:
-            traffic = tr.get("traffic_bytes_per_launch")
-    except (OSError, ValueError):
-        pass
+    dec_ms, pre_ms = statistics.mean(r["dec_ms"]), statistics.mean(r["pre_ms"])
+    src = peak_kind + " (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
+    if pre_ms > dec_ms:  # the prefill kernel dominates: tensor-core roofline
+        flops = prefill_flops(w)
+        achieved = flops / (pre_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "kernel": "pa_prefill_chunk (mma.sync m16n8k16 bf16)",
+                "peak_source": src + " bf16_tflops (burst)"}
+    else:
+        achieved = decode_kv_bytes(w) / (dec_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name),
+                "kernel": "pa_decode (attention + split-K reduce)",
+                "peak_source": src + " hbm_gbs"}
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -404,12 +442,8 @@ def main():
             "e2e": {"value": world * kv_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
             "gpu_launches": r["launches"],
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": traffic,
-                         "kernel": "pa_decode (attention + split-K reduce)",
-                         "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
-                         if peak_kind == "measured" else "fallback 6.8 TB/s"},
+            "roofline": roof,
+            "decode_call_ms": dec_ms, "prefill_call_ms": pre_ms,
             "p10_p50_p90_step_ms": [float(np.percentile(r["step_ms"], p)) for p in (10, 50, 90)]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, nseq, runs, spent = cpu_baseline(w, I, args.cpu_budget)
