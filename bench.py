@@ -214,69 +214,97 @@ def decode_kv_bytes(w):
     return int(eff.sum()) * per_tok * w.num_kv_heads
 
 
+def capture(torch, fn, stream):
+    """CUDA graph of fn's launches (the library's kernels enqueue on the current
+    stream, so they are captured like any other work)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # warm the lazily-set kernel attributes outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_replays(torch, stream, run, n):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(stream)
+        run()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
 def time_ours(args, w, torch, pa, I, rank, world):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     st = DeviceStep(w, torch, pa, I, seed=args.seed + 1000 * rank)
-    stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
+    stream = torch.cuda.Stream()
+
+    def step():
         st.write()
-        st.attend()
-    torch.cuda.synchronize()
+        st.decode()
+        st.prefill()
+
+    if args.no_graph:
+        run_step, run_dec, run_pre = step, st.decode, st.prefill
+    else:
+        g_step = capture(torch, step, stream)
+        g_dec = capture(torch, st.decode, stream)
+        g_pre = capture(torch, st.prefill, stream) if st.max_q else None
+        run_step, run_dec = g_step.replay, g_dec.replay
+        run_pre = g_pre.replay if g_pre else (lambda: None)
     try:
         uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
         uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
     except Exception:
         uuid = None
     clocks = ClockSampler(uuid)
-    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
-    for e0, e1, e2, e3 in ev:
-        e0.record(stream)
-        st.write()
-        e1.record(stream)
-        st.decode()
-        e2.record(stream)
-        st.prefill()
-        e3.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clk = clocks.stop()
-    step_ms = [a.elapsed_time(d) for a, b, c, d in ev]
-    dec_ms = [b.elapsed_time(c) for a, b, c, d in ev]
-    pre_ms = [c.elapsed_time(d) for a, b, c, d in ev] if st.max_q else [0.0]
-    total_ms = sum(step_ms)
-    if int(st.err[0]) != 0:
-        raise RuntimeError("device flags %d during the timed steps" % int(st.err[0]))
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            run_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        clocks.start()
+        time.sleep(0.3)
+        step_ms = time_replays(torch, stream, run_step, args.steps)
+        if world > 1:
+            torch.distributed.barrier()
+        clk = clocks.stop()
+        # the two attention calls on their own, for the per-kernel roofline
+        nk = max(3, min(args.steps, 500))
+        dec_ms = time_replays(torch, stream, run_dec, nk)
+        pre_ms = time_replays(torch, stream, run_pre, nk) if st.max_q else [0.0]
+        torch.cuda.synchronize()
+        if int(st.err[0]) != 0:
+            raise RuntimeError("device flags %d during the timed steps" % int(st.err[0]))
 
-    # end to end: the step's inputs from pinned host memory, its output back
-    host = {name: getattr(st, name).cpu().pin_memory() for name in st.INPUTS}
-    outs = {name: torch.empty(getattr(st, name).shape, dtype=getattr(st, name).dtype
-                              ).pin_memory() for name in st.OUTPUTS}
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for t in outs.values())
-    e2e_steps = max(3, min(args.steps, 200))
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    s0.record(stream)
-    for _ in range(e2e_steps):
-        for name, t in host.items():
-            getattr(st, name).copy_(t, non_blocking=True)
-        st.write()
-        st.attend()
-        for name, t in outs.items():
-            t.copy_(getattr(st, name), non_blocking=True)
-    s1.record(stream)
-    torch.cuda.synchronize()
+        # end to end: the step's inputs from pinned host memory, its output back
+        host = {name: getattr(st, name).cpu().pin_memory() for name in st.INPUTS}
+        outs = {name: torch.empty(getattr(st, name).shape, dtype=getattr(st, name).dtype
+                                  ).pin_memory() for name in st.OUTPUTS}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs.values())
+        e2e_steps = max(3, min(args.steps, 200))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for _ in range(e2e_steps):
+            for name, t in host.items():
+                getattr(st, name).copy_(t, non_blocking=True)
+            run_step()
+            for name, t in outs.items():
+                t.copy_(getattr(st, name), non_blocking=True)
+        s1.record(stream)
+        torch.cuda.synchronize()
     e2e_ms = s0.elapsed_time(s1) / e2e_steps
-    return dict(step_ms=step_ms, dec_ms=dec_ms, pre_ms=pre_ms, total_ms=total_ms, clocks=clk,
-                e2e_ms=e2e_ms,
-                h2d=h2d, d2h=d2h, launches=st.launches_per_step() * args.steps,
-                reduce=st.reduce_launched)
+    return dict(step_ms=step_ms, dec_ms=dec_ms, pre_ms=pre_ms, total_ms=sum(step_ms),
+                clocks=clk, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+                launches=st.launches_per_step() * args.steps, reduce=st.reduce_launched)
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -351,6 +379,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every call from Python instead of replaying a CUDA graph")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="fewer decoding sequences (small profiling captures)")
     args = ap.parse_args()
@@ -432,6 +462,7 @@ def main():
                 "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name),
                 "kernel": "pa_decode (attention + split-K reduce)",
                 "peak_source": src + " hbm_gbs"}
+    cfg["launch"] = "python calls" if args.no_graph else "CUDA graph replay of the step"
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

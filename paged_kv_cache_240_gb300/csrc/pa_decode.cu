@@ -445,47 +445,79 @@ __global__ void __launch_bounds__(kDecThreads, MODE == kI8 ? 5 : 3)
   }
 }
 
-// One warp per (sequence, query head): merge that head's partition states.
+// One 128-thread CTA per (sequence, query head) merges that head's partition
+// states: the maximum and the normaliser over all partitions are reduced by the
+// whole CTA, then each warp accumulates the weighted partial outputs of every
+// fourth partition (lanes across head_dim, several rows in flight) and the four
+// sums are added in shared memory.
+constexpr int kRedThreads = 128;
+
 template <int D, typename QT>
-__global__ void __launch_bounds__(256) pa_reduce_kernel(const AttnParams p, int num_seqs) {
-  const int lane = threadIdx.x & 31;
-  const long long wid = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (wid >= (long long)num_seqs * p.num_q_heads) return;
-  const int b = (int)(wid / p.num_q_heads);
+__global__ void __launch_bounds__(kRedThreads) pa_reduce_kernel(const AttnParams p) {
+  __shared__ float red[kRedThreads / 32];
+  __shared__ float4 part_sum[kRedThreads / 32][D / 4];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long hrow = blockIdx.x;  // b * num_q_heads + h
+  const int b = (int)(hrow / p.num_q_heads);
   const int L = clamp_context(p, b, false);
   if (L == 0) return;
   int lo, first, last;
   const int nparts = decode_parts(p, L, lo, first, last);
   if (nparts <= 1) return;  // written directly by the attention kernel
-  const long long base = wid * p.num_parts;
+  const long long base = hrow * p.num_parts;
+
   float M = -INFINITY;
-  for (int q = 0; q < nparts; q++) M = fmaxf(M, p.ws_m[base + q]);
+  for (int q = threadIdx.x; q < nparts; q += kRedThreads) M = fmaxf(M, p.ws_m[base + q]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+  QT* out = static_cast<QT*>(p.out) + hrow * D;
+  if (M == -INFINITY) {  // no partition saw a key
+    for (int d = threadIdx.x; d < D; d += kRedThreads) out[d] = to_out<QT>(0.0f);
+    return;
+  }
+  float den = 0.0f;
+  for (int q = threadIdx.x; q < nparts; q += kRedThreads)
+    den += exp2f(p.ws_m[base + q] - M) * p.ws_l[base + q];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  if (lane == 0) red[warp] = den;
+
+  // lanes across head_dim: D/32 floats each (a float4 for D = 128, a float2 for 64)
   constexpr int E = D / 32;
-  float acc[E], den = 0.0f;
+  float acc[E];
 #pragma unroll
   for (int e = 0; e < E; e++) acc[e] = 0.0f;
-  if (M != -INFINITY) {
-    for (int q = 0; q < nparts; q++) {
-      const float mq = p.ws_m[base + q];
-      const float w = exp2f(mq - M);  // 0 for a partition with no visible key
-      den += w * p.ws_l[base + q];
-      const float* src = p.ws_o + (base + q) * D + lane * E;
-      if constexpr (E == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-        acc[2] += w * v.z;
-        acc[3] += w * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-      }
+#pragma unroll 4
+  for (int q = warp; q < nparts; q += kRedThreads / 32) {
+    const float w = exp2f(p.ws_m[base + q] - M);  // 0 for a partition with no visible key
+    const float* src = p.ws_o + (base + q) * D + lane * E;
+    if constexpr (E == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] += w * v.x;
+      acc[1] += w * v.y;
+      acc[2] += w * v.z;
+      acc[3] += w * v.w;
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] += w * v.x;
+      acc[1] += w * v.y;
     }
   }
-  QT* out = static_cast<QT*>(p.out) + wid * D + lane * E;
+  float* mine = reinterpret_cast<float*>(&part_sum[warp][0]) + lane * E;
 #pragma unroll
-  for (int e = 0; e < E; e++) out[e] = to_out<QT>(den > 0.0f ? acc[e] / den : 0.0f);
+  for (int e = 0; e < E; e++) mine[e] = acc[e];
+  __syncthreads();
+  const float total = red[0] + red[1] + red[2] + red[3];
+  for (int d = threadIdx.x; d < D; d += kRedThreads) {
+    float v = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kRedThreads / 32; w++) v += reinterpret_cast<const float*>(&part_sum[w][0])[d];
+    out[d] = to_out<QT>(total > 0.0f ? v / total : 0.0f);
+  }
 }
 
 }  // namespace pa_dev
@@ -546,8 +578,8 @@ cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tmk, const CUt
   kern<<<grid, kDecThreads, smem, stream>>>(p, tmk, tmv);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.num_parts <= 1) return e;
-  const long long warps = (long long)num_seqs * p.num_q_heads;
-  pa_reduce_kernel<D, QT><<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(p, num_seqs);
+  const long long heads = (long long)num_seqs * p.num_q_heads;
+  pa_reduce_kernel<D, QT><<<(unsigned)heads, kRedThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

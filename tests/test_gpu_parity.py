@@ -238,3 +238,59 @@ def test_prefill_shapes(dtype, G, D, olib):
     got, flags = run_prefill(w, cache, q, sm, seqs)
     assert flags == 0
     assert_close(got, ref, "%s G=%d D=%d" % (dtype, G, D))
+
+
+def test_cuda_graph_replay_matches_direct_calls():
+    """The calls only enqueue kernels on the caller's stream, so a CUDA graph of
+    a step (write + decode + prefill) replays to the same bits as direct calls."""
+    w = I.make_workload("mixed", seed=31, num_seqs=5, num_chunks=2, chunk_len=70, window=300)
+    kh, vh = I.history_rows(w)
+    nd = w.num_decode
+    new = w.new_slot_mapping()
+    hist_mask = ~np.isin(w.history_slot_mapping(), new)
+    src = I.source_dtype(w)
+    q = bits_to_torch(I.query_rows(w), w.q_dtype)
+    nq = int(w.cu_q_lens[nd])
+    q_dec, q_pre = q[:nq].clone(), q[nq:].clone()
+    k_new = bits_to_torch(kh[~hist_mask], src)
+    v_new = bits_to_torch(vh[~hist_mask], src)
+    slots = i32(w.history_slot_mapping()[~hist_mask])
+    tables_dec, tables_pre = i32(w.block_tables[:nd]), i32(w.block_tables[nd:])
+    lens_dec, lens_pre = i32(w.context_lens[:nd]), i32(w.context_lens[nd:])
+    cu = i32(w.cu_q_lens[nd:] - w.cu_q_lens[nd])
+    sm = 1.0 / np.sqrt(w.head_dim)
+    nbytes = pa.pa_decode_workspace_bytes(nd, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                          w.max_blocks_per_seq, w.window)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+    outs = []
+    for use_graph in (False, True):
+        cache = poisoned_cache(w)
+        err = new_err()
+        hs = w.history_slot_mapping()[hist_mask]
+        pa.pa_write_kv(cache, bits_to_torch(kh[hist_mask], src), bits_to_torch(vh[hist_mask], src),
+                       i32(hs), err)
+        o_dec, o_pre = torch.empty_like(q_dec), torch.empty_like(q_pre)
+        stream = torch.cuda.Stream()
+
+        def step():
+            pa.pa_write_kv(cache, k_new, v_new, slots, err)
+            pa.pa_decode(cache, o_dec, q_dec, tables_dec, lens_dec, sm, w.window, ws, err)
+            pa.pa_prefill_chunk(cache, o_pre, q_pre, cu, int(w.q_lens[nd:].max()), tables_pre,
+                                lens_pre, sm, w.window, err)
+
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            if use_graph:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    step()
+                o_dec.zero_()
+                o_pre.zero_()
+                g.replay()
+            else:
+                step()
+        torch.cuda.synchronize()
+        assert int(err[0]) == 0
+        outs.append((o_dec.clone(), o_pre.clone()))
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
