@@ -143,6 +143,11 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// The tensor-memory kernel for 16-bit caches (pa_prefill_tc.cu).
+template <int D, typename QT>
+cudaError_t launch_prefill_tc(const AttnParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              int num_seqs, cudaStream_t stream);
+
 }  // namespace pa_dev
 
 using namespace pa_dev;
@@ -234,9 +239,20 @@ extern "C" pa_status pa_prefill_chunk(const pa_cache* cache, void* out, const vo
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   const int D = cache->head_dim;
-  if (cache->dtype == PA_F16) e = launch_prefill_d<kF16, __half>(p, tmk, tmv, D, num_seqs, s);
-  else if (cache->dtype == PA_BF16) e = launch_prefill_d<kBF16, __nv_bfloat16>(p, tmk, tmv, D, num_seqs, s);
-  else if (q_dtype == PA_F16) e = launch_prefill_d<kI8, __half>(p, tmk, tmv, D, num_seqs, s);
-  else e = launch_prefill_d<kI8, __nv_bfloat16>(p, tmk, tmv, D, num_seqs, s);
+  if (cache->dtype != PA_I8) {
+    // 16-bit caches: tcgen05 kernel, 128 query rows per CTA
+    p.q_tiles = (int)(((long long)max_q_len * G + 127) / 128);
+    const bool bf = cache->dtype == PA_BF16;
+    if (D == 128)
+      e = bf ? launch_prefill_tc<128, __nv_bfloat16>(p, tmk, tmv, num_seqs, s)
+             : launch_prefill_tc<128, __half>(p, tmk, tmv, num_seqs, s);
+    else
+      e = bf ? launch_prefill_tc<64, __nv_bfloat16>(p, tmk, tmv, num_seqs, s)
+             : launch_prefill_tc<64, __half>(p, tmk, tmv, num_seqs, s);
+  } else if (q_dtype == PA_F16) {
+    e = launch_prefill_d<kI8, __half>(p, tmk, tmv, D, num_seqs, s);
+  } else {
+    e = launch_prefill_d<kI8, __nv_bfloat16>(p, tmk, tmv, D, num_seqs, s);
+  }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
