@@ -454,7 +454,8 @@ def main():
         achieved = flops / (pre_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
-                "kernel": "pa_prefill_chunk (mma.sync m16n8k16 bf16)",
+                "kernel": ("pa_prefill_chunk (tcgen05.mma kind::f16, TMEM accumulators)"
+                           if w.cache_dtype != "i8" else "pa_prefill_chunk (mma.sync m16n8k16)"),
                 "peak_source": src + " bf16_tflops (burst)"}
     else:
         achieved = decode_kv_bytes(w) / (dec_ms * 1e-3) / 1e9

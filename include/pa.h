@@ -210,6 +210,12 @@ pa_status pa_prefill_chunk(const pa_cache *cache, void *out, const void *q, pa_d
 /* Human-readable name of a status. */
 const char *pa_status_str(pa_status status);
 
+/* Text of the CUDA runtime error behind the most recent PA_ERR_CUDA returned to
+ * the calling thread ("no CUDA error" if there was none).  The string is static:
+ * the caller does not free it.  No counterpart in the pages; a diagnostic of the
+ * library's own. */
+const char *pa_last_cuda_error(void);
+
 /* PA_OK when flags == 0, else PA_ERR_DEVICE_DATA (flags read back by the caller). */
 pa_status pa_check_flags(int32_t flags);
 

@@ -19,6 +19,7 @@ __all__ = [
     "pa_prefill_chunk",
     "pa_status_str", "pa_check_flags", "PA_FLAG_SLOT_RANGE", "PA_FLAG_BLOCK_ID",
     "PA_FLAG_CONTEXT_LEN", "PA_FLAG_Q_LEN", "PA_FLAG_TIMEOUT", "EXPORTED_SYMBOLS",
+    "pa_last_cuda_error",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpa_gb300.so")
@@ -30,7 +31,7 @@ PA_FLAG_SLOT_RANGE, PA_FLAG_BLOCK_ID, PA_FLAG_CONTEXT_LEN, PA_FLAG_Q_LEN, PA_FLA
 
 EXPORTED_SYMBOLS = ("pa_write_kv", "pa_decode", "pa_decode_partitioned",
                     "pa_decode_workspace_bytes", "pa_decode_noalloc", "pa_prefill_chunk",
-                    "pa_status_str", "pa_check_flags")
+                    "pa_status_str", "pa_last_cuda_error", "pa_check_flags")
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -72,6 +73,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_status_str.argtypes = [I]
     lib.pa_status_str.restype = ctypes.c_char_p
     lib.pa_check_flags.argtypes = [ctypes.c_int32]
+    lib.pa_last_cuda_error.argtypes = []
+    lib.pa_last_cuda_error.restype = ctypes.c_char_p
     for name in ("pa_write_kv", "pa_decode", "pa_decode_partitioned", "pa_decode_noalloc",
                  "pa_prefill_chunk", "pa_check_flags"):
         getattr(lib, name).restype = I
@@ -89,6 +92,11 @@ def _status_name(status: int) -> str:
 
 def pa_status_str(status: int) -> str:
     return load_library().pa_status_str(int(status)).decode()
+
+
+def pa_last_cuda_error() -> str:
+    """Text of the CUDA error behind this thread's most recent PA_ERR_CUDA."""
+    return load_library().pa_last_cuda_error().decode()
 
 
 def pa_check_flags(flags: int) -> int:
@@ -135,6 +143,8 @@ def _check_cuda(*ts):
 
 
 def _raise(status: int, what: str):
+    if status == PA_ERR_CUDA:
+        raise PaError(status, "%s (%s)" % (what, load_library().pa_last_cuda_error().decode()))
     if status != PA_OK:
         raise PaError(status, what)
 

@@ -354,12 +354,12 @@ __global__ void __launch_bounds__(kDecThreads, MODE == kI8 ? 5 : 3)
     kcorr[1] = 1152.0f * __shfl_sync(0xffffffffu, qs, 8 * t + 4);
   }
 
-  bool timed_out = false;
+  int kfail = -1;  // the block whose wait ran out
   for (int k = 0; k < nmine; k++) {
     const int slot = warp + kDecWarps * (k & 1);
     if (!mbar_wait(&s.full[slot], (k >> 1) & 1)) {
       if (lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
-      timed_out = true;
+      kfail = k;
       break;
     }
     if (s.valid[slot])
@@ -375,8 +375,10 @@ __global__ void __launch_bounds__(kDecThreads, MODE == kI8 ? 5 : 3)
                            kvh, lane);
     }
   }
-  if (timed_out) {  // no copy may still be landing in shared memory when the CTA exits
-    for (int k = 0; k < nmine; k++)
+  if (kfail >= 0) {  // no copy may still be landing in shared memory when the CTA exits
+    // only blocks kfail and kfail+1 can be in flight, and they are their stages'
+    // current phases (a parity wait cannot tell an older phase from the current one)
+    for (int k = kfail; k < nmine && k < kfail + 2; k++)
       if (!mbar_wait(&s.full[warp + kDecWarps * (k & 1)], (k >> 1) & 1)) break;
     if (lane == 0) *s.abort_flag = 1;
   }
@@ -673,7 +675,7 @@ extern "C" pa_status pa_decode_partitioned(const pa_cache* cache, void* out, con
   CUtensorMap tmk, tmv;
   if (!pa_internal::encode_cache_map(&tmk, cache, cache->k_cache) ||
       !pa_internal::encode_cache_map(&tmv, cache, cache->v_cache))
-    return PA_ERR_CUDA;
+    return pa_internal::cuda_status(cudaErrorInvalidValue);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   const int D = cache->head_dim;
@@ -681,7 +683,7 @@ extern "C" pa_status pa_decode_partitioned(const pa_cache* cache, void* out, con
   else if (cache->dtype == PA_BF16) e = launch_decode_d<kBF16, __nv_bfloat16>(p, tmk, tmv, D, num_seqs, s);
   else if (q_dtype == PA_F16) e = launch_decode_d<kI8, __half>(p, tmk, tmv, D, num_seqs, s);
   else e = launch_decode_d<kI8, __nv_bfloat16>(p, tmk, tmv, D, num_seqs, s);
-  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return pa_internal::cuda_status(e);
 }
 
 extern "C" pa_status pa_decode(const pa_cache* cache, void* out, const void* q, pa_dtype q_dtype,
@@ -717,13 +719,15 @@ void* g_noalloc_addr[kMaxDevices];  // device address of the scratch, per device
 
 pa_status noalloc_scratch(void** addr) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return pa_internal::cuda_status(e);
   if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc_addr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return PA_ERR_CUDA;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return pa_internal::cuda_status(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
     g_noalloc_addr[dev] = p;
   }
   *addr = g_noalloc_addr[dev];

@@ -9,6 +9,15 @@
 
 namespace pa_internal {
 
+// Records the CUDA error behind a PA_ERR_CUDA for pa_last_cuda_error (per
+// calling thread) and returns the status to hand back.
+void record_cuda_error(cudaError_t e);
+inline pa_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return PA_OK;
+  record_cuda_error(e);
+  return PA_ERR_CUDA;
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Checks every field of the cache description; nothing is dereferenced on the

@@ -235,13 +235,12 @@ extern "C" pa_status pa_prefill_chunk(const pa_cache* cache, void* out, const vo
   CUtensorMap tmk, tmv;
   if (!pa_internal::encode_cache_map(&tmk, cache, cache->k_cache) ||
       !pa_internal::encode_cache_map(&tmv, cache, cache->v_cache))
-    return PA_ERR_CUDA;
+    return pa_internal::cuda_status(cudaErrorInvalidValue);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   const int D = cache->head_dim;
   if (cache->dtype != PA_I8) {
-    // 16-bit caches: tcgen05 kernel, 128 query rows per CTA
-    p.q_tiles = (int)(((long long)max_q_len * G + 127) / 128);
+    // 16-bit caches: tcgen05 kernel (sizes its own grid)
     const bool bf = cache->dtype == PA_BF16;
     if (D == 128)
       e = bf ? launch_prefill_tc<128, __nv_bfloat16>(p, tmk, tmv, num_seqs, s)
@@ -254,5 +253,5 @@ extern "C" pa_status pa_prefill_chunk(const pa_cache* cache, void* out, const vo
   } else {
     e = launch_prefill_d<kI8, __nv_bfloat16>(p, tmk, tmv, D, num_seqs, s);
   }
-  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return pa_internal::cuda_status(e);
 }

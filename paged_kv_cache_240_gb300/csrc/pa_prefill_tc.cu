@@ -3,19 +3,23 @@
 // ("PyTorch LLM Serving Engine", "What is implemented": chunked prefill; "Loading":
 // online softmax while walking the block table).
 //
-// A CTA owns 128 query rows of one sequence's chunk and one kv head: row
-// R = c*G + j is query token c, query head kvh*G + j.  The keys the rows can see
-// are walked in tiles of 64 (four 16-token blocks):
+// A CTA owns 256 query rows (two tiles of 128) of one sequence's chunk and one
+// kv head: row R = c*G + j is query token c, query head kvh*G + j.  The keys the
+// rows can see are walked in tiles of 64 (four 16-token blocks), each tile used
+// by both query tiles:
 //   S_t  = Q K_t^T      tcgen05.mma M=128 N=64  K=head_dim -> TMEM (two buffers)
 //   P_t  = exp2(S_t*scale - m)   one softmax thread per row, written to shared
 //                                memory as f16/bf16 in the MMA's K-major layout
 //   O   += P_t V_t      tcgen05.mma M=128 N=head_dim K=64 -> TMEM
 // Warps: 0 = TMA producer (paged K/V tiles into a ring of stages), 1 = MMA
-// issuer (one thread) and tensor-memory owner, 2..5 = softmax, one TMEM lane
-// (row) per thread.  The running maximum is rescaled lazily: O (in TMEM) and the
-// normaliser are only rescaled when a row's maximum grows by more than 2^8, so
-// the exponentials stay below 256.  Every barrier is waited on at most one phase
-// behind its current phase, and every wait is bounded.
+// issuer (one thread) and tensor-memory owner, 2..5 and 6..9 = softmax for query
+// tiles 0 and 1, one TMEM lane (row) per thread; the two softmax warpgroups run
+// in parallel, so one tile's exponentials overlap the other tile's MMAs.  The
+// running maximum is rescaled lazily: O (in TMEM) and the normaliser are only
+// rescaled when a row's maximum grows by more than 2^8, so the exponentials stay
+// below 256.  A parity wait only tells a barrier's current phase from the one
+// before, so every barrier is waited on at every phase, in order; every wait is
+// bounded.
 #include <algorithm>
 
 #include "pa_attn_common.cuh"
@@ -24,37 +28,57 @@
 namespace pa_dev {
 namespace tc {
 
-constexpr int kRows = 128;      // query rows per CTA (MMA M)
+constexpr int kRows = 128;      // query rows per tile (MMA M)
+constexpr int kQTiles = 2;      // query tiles per CTA
+constexpr int kCtaRows = kQTiles * kRows;
 constexpr int kKeys = 64;       // keys per tile (MMA N of S, K of P V)
 constexpr int kTileBlocks = kKeys / kBlock;
 constexpr int kNS = 3;          // K/V stages
-constexpr int kThreads = 192;   // 6 warps
-constexpr int kSoftmaxThreads = 128;
+constexpr int kSoftmaxThreads = 128;  // per query tile
+constexpr int kThreads = 64 + kQTiles * kSoftmaxThreads;  // 10 warps
 constexpr float kLazyRescale = 8.0f;  // log2 of the growth that forces a rescale
+constexpr float kNoMax = -1.0e30f;    // running-maximum sentinel: 2^(-inf - kNoMax) = 0
 
 template <int D>
 struct Layout {
   static constexpr int kChunks = D / 64;               // 128-byte chunks of a row
-  static constexpr int kQBytes = kRows * D * 2;        // [chunk][128 rows][128 B]
+  static constexpr int kQBytes = kRows * D * 2;        // per tile: [chunk][128 rows][128 B]
   static constexpr int kKVChunk = kKeys * 128;         // one chunk of a K or V tile
   static constexpr int kKVBytes = kChunks * kKVChunk;  // [chunk][64 rows][128 B]
   static constexpr int kStageBytes = 2 * kKVBytes;     // K then V
   static constexpr int kPBytes = kRows * kKeys * 2;    // [128 rows][128 B]
   static constexpr int kQOff = 0;
-  static constexpr int kStageOff = kQOff + kQBytes;
-  static constexpr int kPOff = kStageOff + kNS * kStageBytes;
-  static constexpr int kBarOff = kPOff + 2 * kPBytes;
-  // barriers: kv_full[NS], kv_free[NS], s_full[2], s_free[2], p_full[2], p_free[2], o_done, q_full
-  static constexpr int kNumBars = 2 * kNS + 8 + 2;
+  static constexpr int kStageOff = kQOff + kQTiles * kQBytes;
+  static constexpr int kPOff = kStageOff + kNS * kStageBytes;  // [tile][buffer]
+  static constexpr int kBarOff = kPOff + kQTiles * 2 * kPBytes;
+  // barriers: kv_full[NS], kv_free[NS], q_full, then per query tile s_full[2],
+  // s_free[2], p_full[2], o_done
+  static constexpr int kTileBars = 7;
+  static constexpr int kNumBars = 2 * kNS + 1 + kQTiles * kTileBars;
   static constexpr int kFlagOff = kBarOff + kNumBars * 8;  // valid flags [NS][4] ints
   static constexpr int kTmemSlotOff = kFlagOff + kNS * kTileBlocks * 4;
   static constexpr int kUsed = kTmemSlotOff + 16;
   static constexpr int kBytes = kUsed + 1024;  // room to align the base to 1024
-  // tensor memory columns: S buffers 0/1, then O
+  // tensor memory columns per query tile: S buffers 0/1, then O
   static constexpr uint32_t kSCol0 = 0, kSCol1 = kKeys, kOCol = 2 * kKeys;
-  static constexpr uint32_t kTmemCols = 256;
-  static_assert(kOCol + D <= kTmemCols, "tensor memory budget");
+  static constexpr uint32_t kTileCols = 256;
+  static constexpr uint32_t kTmemCols = kQTiles * kTileCols;
+  static_assert(kOCol + D <= kTileCols, "tensor memory budget");
+  static_assert(kBytes <= 232448, "shared memory budget");
 };
+
+struct TileBars {
+  uint64_t *s_full, *s_free, *p_full, *o_done;
+};
+
+__device__ __forceinline__ TileBars tile_bars(uint64_t* base) {
+  TileBars b;
+  b.s_full = base;
+  b.s_free = base + 2;
+  b.p_full = base + 4;
+  b.o_done = base + 6;
+  return b;
+}
 
 // Shared-memory matrix descriptor, 128-byte swizzle (sm_100 family layout:
 // start >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride byte
@@ -152,12 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::kBarOff);
   uint64_t* kv_full = bars;
   uint64_t* kv_free = bars + kNS;
-  uint64_t* s_full = bars + 2 * kNS;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_full + 4;
-  uint64_t* p_free = s_full + 6;
-  uint64_t* o_done = s_full + 8;
-  uint64_t* q_full = s_full + 9;
+  uint64_t* q_full = bars + 2 * kNS;
+  uint64_t* tbar0 = q_full + 1;  // per-tile barriers follow
   int* vflags = reinterpret_cast<int*>(smem + LY::kFlagOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::kTmemSlotOff);
 
@@ -180,11 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int L = clamp_context(p, n, reporter);
   if (C > L && reporter) set_flag(p.err, PA_FLAG_Q_LEN);
-  const int R0 = tile * kRows;
+  const int R0 = tile * kCtaRows;
   const int nrows = C * G;
   if (R0 >= nrows) return;
   const int c_first = R0 / G;
-  const int c_last = (min(R0 + kRows, nrows) - 1) / G;
+  const int c_last = (min(R0 + kCtaRows, nrows) - 1) / G;
   const int hi_u = L - C + c_last;
   const int lo_u = p.window > 0 ? max(0, L - C + c_first - p.window + 1) : 0;
   const int first = lo_u / kBlock;
@@ -192,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = hi_u >= lo_u ? (last - first) / kTileBlocks + 1 : 0;
   QT* out = static_cast<QT*>(p.out);
   if (ntiles == 0) {  // no row sees a key: zeros
-    for (int idx = threadIdx.x; idx < kRows * D; idx += kThreads) {
+    for (int idx = threadIdx.x; idx < kCtaRows * D; idx += kThreads) {
       const int R = R0 + idx / D;
       if (R < nrows)
         out[((long long)(q0 + R / G) * p.num_q_heads + kvh * G + R % G) * D + idx % D] =
@@ -206,17 +226,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_free[i], 1);
     }
-    for (int i = 0; i < 2; i++) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], kSoftmaxThreads);
-      mbar_init(&p_full[i], kSoftmaxThreads);
-      mbar_init(&p_free[i], 1);
+    mbar_init(q_full, kQTiles * kSoftmaxThreads);
+    for (int q = 0; q < kQTiles; q++) {
+      const TileBars tb = tile_bars(tbar0 + q * LY::kTileBars);
+      for (int i = 0; i < 2; i++) {
+        mbar_init(&tb.s_full[i], 1);
+        mbar_init(&tb.s_free[i], kSoftmaxThreads);
+        mbar_init(&tb.p_full[i], kSoftmaxThreads);
+      }
+      mbar_init(tb.o_done, 1);
     }
-    mbar_init(o_done, 1);
-    mbar_init(q_full, kSoftmaxThreads);
     fence_mbar_init();
   }
-  if (warp == 1) {  // tensor memory for S (2 x 64 columns) and O (head_dim columns)
+  if (warp == 1) {  // tensor memory: per query tile, S (2 x 64 columns) and O
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(LY::kTmemCols));
@@ -232,7 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- producer: K/V tiles of four blocks each
     const int32_t* table = p.block_tables + (long long)n * p.max_blocks_per_seq + first;
     const int nblk = last - first + 1;
-    for (int t = 0; t < ntiles && !timed_out; t++) {
+    int issued = 0;
+    for (int t = 0; t < ntiles && !timed_out; t++, issued++) {
       const int st = t % kNS;
       if (t >= kNS && !mbar_wait(&kv_free[st], ((t / kNS) - 1) & 1)) {
         timed_out = true;
@@ -247,11 +270,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();  // every lane's flag is written before lane 0 arms the stage
       const unsigned okmask = __ballot_sync(0xffffffffu, ok);
-      if (lane == 0) {
+      if (lane == 0)
         mbar_arrive_expect_tx(&kv_full[st], __popc(okmask) * 2u * LY::kKVBytes / kTileBlocks);
-      }
       __syncwarp();
-      if (ok && lane < kTileBlocks) {
+      if (ok) {
         uint8_t* kbase = smem + LY::kStageOff + st * LY::kStageBytes;
         uint8_t* vbase = kbase + LY::kKVBytes;
         const int row0 = (mine * p.num_kv_heads + kvh) * kBlock;
@@ -264,113 +286,153 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    // no copy may still be landing in shared memory when the CTA exits
+    // no copy may still be landing in shared memory when the CTA exits; the last
+    // kNS tiles issued are their stages' current phases
     if (lane == 0)
-      for (int t = ntiles > kNS ? ntiles - kNS : 0; t < ntiles; t++)
+      for (int t = issued > kNS ? issued - kNS : 0; t < issued; t++)
         if (!mbar_wait(&kv_full[t % kNS], (t / kNS) & 1)) break;
+    if (timed_out && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
   } else if (warp == 1) {
     // ---------------- MMA issuer (one thread)
     if (lane == 0) {
-      const uint32_t sQ = smem_u32(smem + LY::kQOff);
       const uint32_t idS = idesc<BF>(kRows, kKeys, false);
       const uint32_t idO = idesc<BF>(kRows, D, true);
-      auto pv = [&](int t) -> bool {  // O += P_t V_t
-        if (!mbar_wait(&p_full[t & 1], (t >> 1) & 1)) return false;
+      auto pv = [&](int q, int t) -> bool {  // O_q += P_{q,t} V_t
+        const TileBars tb = tile_bars(tbar0 + q * LY::kTileBars);
+        if (!mbar_wait(&tb.p_full[t & 1], (t >> 1) & 1)) return false;
         fence_after();
-        const uint32_t sP = smem_u32(smem + LY::kPOff + (t & 1) * LY::kPBytes);
+        const uint32_t sP = smem_u32(smem + LY::kPOff + (2 * q + (t & 1)) * LY::kPBytes);
         const uint32_t sV = smem_u32(smem + LY::kStageOff + (t % kNS) * LY::kStageBytes) +
                             LY::kKVBytes;
+        const uint32_t dO = tmem + q * LY::kTileCols + LY::kOCol;
 #pragma unroll
         for (int s = 0; s < kKeys / 16; s++)
-          mma(tmem + LY::kOCol, sw128_desc(sP + 32 * s, 16, 1024),
+          mma(dO, sw128_desc(sP + 32 * s, 16, 1024),
               sw128_desc(sV + 2048 * s, LY::kKVChunk, 1024), idO, (t > 0 || s > 0) ? 1u : 0u);
-        commit(&p_free[t & 1]);
-        commit(o_done);
-        commit(&kv_free[t % kNS]);
+        commit(tb.o_done);
         return true;
       };
       bool ok = mbar_wait(q_full, 0);
       for (int t = 0; t < ntiles && ok; t++) {
         const int st = t % kNS;
         ok = mbar_wait(&kv_full[st], (t / kNS) & 1);
-        if (ok && t >= 2) ok = mbar_wait(&s_free[t & 1], ((t - 2) >> 1) & 1);
-        if (!ok) break;
-        fence_after();
         const uint32_t sK = smem_u32(smem + LY::kStageOff + st * LY::kStageBytes);
-        const uint32_t dS = tmem + ((t & 1) ? LY::kSCol1 : LY::kSCol0);
+        for (int q = 0; q < kQTiles && ok; q++) {
+          const TileBars tb = tile_bars(tbar0 + q * LY::kTileBars);
+          if (t >= 2) ok = mbar_wait(&tb.s_free[t & 1], ((t - 2) >> 1) & 1);
+          if (!ok) break;
+          fence_after();
+          const uint32_t sQ = smem_u32(smem + LY::kQOff + q * LY::kQBytes);
+          const uint32_t dS = tmem + q * LY::kTileCols + ((t & 1) ? LY::kSCol1 : LY::kSCol0);
 #pragma unroll
-        for (int s = 0; s < D / 16; s++)
-          mma(dS, sw128_desc(sQ + (s / 4) * (kRows * 128) + (s % 4) * 32, 16, 1024),
-              sw128_desc(sK + (s / 4) * LY::kKVChunk + (s % 4) * 32, 16, 1024), idS,
-              s > 0 ? 1u : 0u);
-        commit(&s_full[t & 1]);
-        if (t >= 1) ok = pv(t - 1);
+          for (int s = 0; s < D / 16; s++)
+            mma(dS, sw128_desc(sQ + (s / 4) * (kRows * 128) + (s % 4) * 32, 16, 1024),
+                sw128_desc(sK + (s / 4) * LY::kKVChunk + (s % 4) * 32, 16, 1024), idS,
+                s > 0 ? 1u : 0u);
+          commit(&tb.s_full[t & 1]);
+        }
+        if (ok && t >= 1) {
+          for (int q = 0; q < kQTiles && ok; q++) ok = pv(q, t - 1);
+          if (ok) commit(&kv_free[(t - 1) % kNS]);
+        }
       }
-      if (ok) ok = pv(ntiles - 1);
+      if (ok) {
+        for (int q = 0; q < kQTiles && ok; q++) ok = pv(q, ntiles - 1);
+        if (ok) commit(&kv_free[(ntiles - 1) % kNS]);
+      }
       if (!ok) set_flag(p.err, PA_FLAG_TIMEOUT);
     }
     __syncwarp();
   } else {
-    // ---------------- softmax: thread <-> row (TMEM lane 32*(warp%4) + lane)
+    // ---------------- softmax: query tile q, thread <-> row (TMEM lane 32*(warp%4) + lane)
+    const int q = (warp - 2) / 4;
+    const TileBars tb = tile_bars(tbar0 + q * LY::kTileBars);
+    const int stid = threadIdx.x - 64 - q * kSoftmaxThreads;  // 0..127 within the tile
     const int row = 32 * (warp & 3) + lane;
-    const int R = R0 + row;
+    const int R = R0 + q * kRows + row;
     const bool rvalid = R < nrows;
     const int c = rvalid ? R / G : 0;
     const int pos = L - C + c;
     const int row_hi = rvalid ? pos : -1;
     const int row_lo = p.window > 0 ? max(0, pos - p.window + 1) : 0;
     const long long orow = (long long)(q0 + c) * p.num_q_heads + kvh * G + (rvalid ? R % G : 0);
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const uint32_t lane_base = tmem + q * LY::kTileCols + ((uint32_t)(32 * (warp & 3)) << 16);
+    const float sc = p.scale_log2;
 
     // Q row -> shared memory in the MMA's swizzled K-major layout
     {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const QT*>(p.q) + orow * D);
+      uint8_t* qt = smem + LY::kQOff + q * LY::kQBytes;
 #pragma unroll
       for (int u = 0; u < D / 8; u++) {
         const uint4 v = rvalid ? src[u] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(smem + LY::kQOff + (u / 8) * (kRows * 128) + sw_unit(row, u % 8)) = v;
+        *reinterpret_cast<uint4*>(qt + (u / 8) * (kRows * 128) + sw_unit(row, u % 8)) = v;
       }
       fence_proxy_async();
       mbar_arrive(q_full);
     }
 
-    float m_used = -INFINITY, l = 0.0f;
+    // o_done completes once per P V of this tile.  It is waited on at every key
+    // tile t >= 1 (for the P V of tile t-1): early when O must be rescaled,
+    // otherwise just before P is written; waiting again on that same, completed
+    // phase returns at once, and the barrier cannot move on before this tile's
+    // P is published.
+    float m_used = kNoMax, l = 0.0f;
     for (int t = 0; t < ntiles; t++) {
-      if (!mbar_wait(&s_full[t & 1], (t >> 1) & 1)) {
+      if (!mbar_wait(&tb.s_full[t & 1], (t >> 1) & 1)) {
         timed_out = true;
         break;
       }
       fence_after();
       const int pos0 = (first + kTileBlocks * t) * kBlock;
       const int* vf = vflags + (t % kNS) * kTileBlocks;
+      const bool blocks_ok = vf[0] && vf[1] && vf[2] && vf[3];
       float x[kKeys];
       {
         float v[32];
-        const uint32_t sc = (t & 1) ? LY::kSCol1 : LY::kSCol0;
-        tmem_ld32(lane_base + sc, v);
+        const uint32_t scol = (t & 1) ? LY::kSCol1 : LY::kSCol0;
+        tmem_ld32(lane_base + scol, v);
 #pragma unroll
         for (int i = 0; i < 32; i++) x[i] = v[i];
-        tmem_ld32(lane_base + sc + 32, v);
+        tmem_ld32(lane_base + scol + 32, v);
 #pragma unroll
         for (int i = 0; i < 32; i++) x[32 + i] = v[i];
       }
       fence_before();
-      mbar_arrive(&s_free[t & 1]);  // the MMA may overwrite this S buffer now
-      float mt = -INFINITY;
+      mbar_arrive(&tb.s_free[t & 1]);  // the MMA may overwrite this S buffer now
+      // maximum of the scaled scores this row can see; an inner tile (every key
+      // visible to every row of the warp) skips the masks.  Eight partial maxima
+      // and sums keep the dependency chains short.
+      float part[8];
+      const bool inner = __all_sync(0xffffffffu, blocks_ok && pos0 >= row_lo &&
+                                                     pos0 + kKeys - 1 <= row_hi) &&
+                         sc > 0.0f;
+      if (inner) {
 #pragma unroll
-      for (int i = 0; i < kKeys; i++) {
-        const int kp = pos0 + i;
-        const bool vis = kp >= row_lo && kp <= row_hi && vf[i / kBlock];
-        x[i] = vis ? x[i] * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, x[i]);
+        for (int j = 0; j < 8; j++) part[j] = x[j];
+#pragma unroll
+        for (int i = 8; i < kKeys; i++) part[i & 7] = fmaxf(part[i & 7], x[i]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; j++) part[j] = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kKeys; i++) {
+          const int kp = pos0 + i;
+          const bool vis = kp >= row_lo && kp <= row_hi && vf[i / kBlock];
+          x[i] = vis ? x[i] * sc : -INFINITY;
+          part[i & 7] = fmaxf(part[i & 7], x[i]);
+        }
       }
+      float mt = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
+                       fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
+      if (inner) mt *= sc;
       // lazy rescale: only when this row's maximum grew by more than 2^8
       const bool need = mt > m_used + kLazyRescale;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? mt : m_used;
-        const float factor = (need && m_used != -INFINITY) ? fast_exp2(m_used - m_new) : (need ? 0.0f : 1.0f);
+        const float factor = need ? fast_exp2(m_used - m_new) : 1.0f;
         if (t > 0) {  // O holds tiles < t: wait for the last P V, then scale it in place
-          if (!mbar_wait(o_done, (t - 1) & 1)) {
+          if (!mbar_wait(tb.o_done, (t - 1) & 1)) {
             timed_out = true;
             break;
           }
@@ -387,36 +449,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= factor;
         m_used = m_new;
       }
-      // P row -> shared memory (bf16/f16, K-major swizzled), after the P V two
-      // tiles back has finished reading this buffer
-      if (t >= 2 && !mbar_wait(&p_free[t & 1], ((t - 2) >> 1) & 1)) {
+      // inner tiles hold raw scores (the scale is folded into one FFMA), edge
+      // tiles already-scaled ones (-inf where masked)
+      const float mul = inner ? sc : 1.0f;
+      const float sub = -m_used;
+#pragma unroll
+      for (int j = 0; j < 8; j++) part[j] = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kKeys; i++) {
+        x[i] = fast_exp2(fmaf(x[i], mul, sub));
+        part[i & 7] += x[i];
+      }
+      l += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+      // the P V of tile t-1 has finished: O is settled, and P buffer t&1 (last
+      // read by the P V of tile t-2) is free
+      if (t > 0 && !mbar_wait(tb.o_done, (t - 1) & 1)) {
         timed_out = true;
         break;
       }
-      uint8_t* prow = smem + LY::kPOff + (t & 1) * LY::kPBytes;
-      float ls = 0.0f;
+      // P row -> shared memory (f16/bf16, K-major swizzled)
+      uint8_t* prow = smem + LY::kPOff + (2 * q + (t & 1)) * LY::kPBytes;
 #pragma unroll
       for (int u = 0; u < kKeys / 8; u++) {
-        float e[8];
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-          e[i] = m_used == -INFINITY ? 0.0f : fast_exp2(x[8 * u + i] - m_used);
-          ls += e[i];
-        }
         uint4 pk;
-        pk.x = pack2<BF>(e[0], e[1]);
-        pk.y = pack2<BF>(e[2], e[3]);
-        pk.z = pack2<BF>(e[4], e[5]);
-        pk.w = pack2<BF>(e[6], e[7]);
+        pk.x = pack2<BF>(x[8 * u + 0], x[8 * u + 1]);
+        pk.y = pack2<BF>(x[8 * u + 2], x[8 * u + 3]);
+        pk.z = pack2<BF>(x[8 * u + 4], x[8 * u + 5]);
+        pk.w = pack2<BF>(x[8 * u + 6], x[8 * u + 7]);
         *reinterpret_cast<uint4*>(prow + sw_unit(row, u)) = pk;
       }
-      l += ls;
       // V rows of keys no row can see (before the window, past the context,
-      // blocks not in the pool) may hold garbage: zero them so 0 * V stays 0
-      const bool edge = pos0 < lo_u || pos0 + kKeys - 1 > hi_u || !(vf[0] && vf[1] && vf[2] && vf[3]);
-      if (edge) {
+      // blocks not in the pool) may hold garbage: zero them so 0 * V stays 0.
+      // Both query tiles read the stage; tile 0's warps clear it, and the MMA
+      // thread waits for tile 0's P before either tile's P V.
+      const bool edge = pos0 < lo_u || pos0 + kKeys - 1 > hi_u || !blocks_ok;
+      if (edge && q == 0) {
         uint8_t* vbase = smem + LY::kStageOff + (t % kNS) * LY::kStageBytes + LY::kKVBytes;
-        for (int idx = threadIdx.x - 64; idx < kKeys * LY::kChunks * 8; idx += kSoftmaxThreads) {
+        for (int idx = stid; idx < kKeys * LY::kChunks * 8; idx += kSoftmaxThreads) {
           const int key = idx / (LY::kChunks * 8);
           const int rest = idx % (LY::kChunks * 8);
           const int kp = pos0 + key;
@@ -427,10 +496,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async();
       fence_before();
-      mbar_arrive(&p_full[t & 1]);
+      mbar_arrive(&tb.p_full[t & 1]);
     }
-    // epilogue: wait for the last P V, then O / l
-    if (!timed_out && mbar_wait(o_done, (ntiles - 1) & 1)) {
+    // epilogue: wait for the last P V (its predecessor was waited at the last tile)
+    if (!timed_out && mbar_wait(tb.o_done, (ntiles - 1) & 1)) {
       fence_after();
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
       QT* dst = out + orow * D;
@@ -472,8 +541,10 @@ cudaError_t launch_prefill_tc(const AttnParams& p, const CUtensorMap& tmk,
   auto kern = tc::pa_prefill_tc_kernel<D, QT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)(p.q_tiles * p.num_kv_heads), (unsigned)num_seqs);
-  kern<<<grid, tc::kThreads, smem, stream>>>(p, tmk, tmv);
+  AttnParams pt = p;
+  pt.q_tiles = (int)(((long long)p.max_q_len * p.group + tc::kCtaRows - 1) / tc::kCtaRows);
+  const dim3 grid((unsigned)(pt.q_tiles * pt.num_kv_heads), (unsigned)num_seqs);
+  kern<<<grid, tc::kThreads, smem, stream>>>(pt, tmk, tmv);
   return cudaGetLastError();
 }
 

@@ -1,5 +1,18 @@
 // pa_status.cu -- status helpers of the C ABI.
+#include <cuda_runtime.h>
+
 #include "pa.h"
+#include "pa_internal.h"
+
+namespace {
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+}
+
+void pa_internal::record_cuda_error(cudaError_t e) { g_last_cuda_error = e; }
+
+extern "C" const char* pa_last_cuda_error(void) {
+  return g_last_cuda_error == cudaSuccess ? "no CUDA error" : cudaGetErrorString(g_last_cuda_error);
+}
 
 extern "C" const char* pa_status_str(pa_status status) {
   switch (status) {

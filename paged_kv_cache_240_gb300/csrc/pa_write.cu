@@ -178,5 +178,5 @@ extern "C" pa_status pa_write_kv(const pa_cache* cache, const void* k, const voi
     if (d128) write_quant_kernel<__nv_bfloat16, 128><<<g, b, 0, s>>>(p);
     else write_quant_kernel<__nv_bfloat16, 64><<<g, b, 0, s>>>(p);
   }
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return pa_internal::cuda_status(cudaGetLastError());
 }

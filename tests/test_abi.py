@@ -44,6 +44,7 @@ def test_status_strings(lib):
     assert pa.pa_status_str(4) == "PA_ERR_DEVICE_DATA"
     assert pa.pa_check_flags(0) == 0
     assert pa.pa_check_flags(pa.PA_FLAG_BLOCK_ID) == 4
+    assert pa.pa_last_cuda_error() == "no CUDA error"  # nothing has failed on this thread
 
 
 def _cache(**kw):
