@@ -12,7 +12,8 @@
 //                                memory as f16/bf16 in the MMA's K-major layout
 //   O   += P_t V_t      tcgen05.mma M=128 N=head_dim K=64 -> TMEM
 // Warps: 0 = TMA producer (paged K/V tiles into a ring of stages), 1 = MMA
-// issuer (one thread) and tensor-memory owner, 2..5 and 6..9 = softmax for query
+// issuer (the warp runs the schedule, one elected lane issues) and tensor-memory
+// owner, 2..5 and 6..9 = softmax for query
 // tiles 0 and 1, one TMEM lane (row) per thread; the two softmax warpgroups run
 // in parallel, so one tile's exponentials overlap the other tile's MMAs.  The
 // running maximum is rescaled lazily: O (in TMEM) and the normaliser are only
@@ -52,8 +53,8 @@ struct Layout {
   static constexpr int kPOff = kStageOff + kNS * kStageBytes;  // [tile][buffer]
   static constexpr int kBarOff = kPOff + kQTiles * 2 * kPBytes;
   // barriers: kv_full[NS], kv_free[NS], q_full, then per query tile s_full[2],
-  // s_free[2], p_full[2], o_done
-  static constexpr int kTileBars = 7;
+  // s_free[2], p_full[2], p_free[2]
+  static constexpr int kTileBars = 8;
   static constexpr int kNumBars = 2 * kNS + 1 + kQTiles * kTileBars;
   static constexpr int kFlagOff = kBarOff + kNumBars * 8;  // valid flags [NS][4] ints
   static constexpr int kTmemSlotOff = kFlagOff + kNS * kTileBlocks * 4;
@@ -68,7 +69,7 @@ struct Layout {
 };
 
 struct TileBars {
-  uint64_t *s_full, *s_free, *p_full, *o_done;
+  uint64_t *s_full, *s_free, *p_full, *p_free;
 };
 
 __device__ __forceinline__ TileBars tile_bars(uint64_t* base) {
@@ -76,7 +77,7 @@ __device__ __forceinline__ TileBars tile_bars(uint64_t* base) {
   b.s_full = base;
   b.s_free = base + 2;
   b.p_full = base + 4;
-  b.o_done = base + 6;
+  b.p_free = base + 6;
   return b;
 }
 
@@ -97,19 +98,27 @@ __host__ __device__ constexpr uint32_t idesc(int M, int N, bool b_mn_major) {
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
-                                    uint32_t accumulate) {
+// The MMA warp runs its schedule with all 32 lanes, so the descriptors stay
+// warp-uniform, and one elected lane issues each MMA and commit.
+__device__ __forceinline__ void mma_elect(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                          uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(id), "r"(accumulate));
 }
 
-__device__ __forceinline__ void commit(uint64_t* bar) {
+__device__ __forceinline__ void commit_elect(uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
           smem_u32(bar))
       : "memory");
+}
+
+// Bounded wait by every lane of a warp; the verdict is the warp's (uniform).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
 __device__ __forceinline__ void fence_before() {
@@ -233,8 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&tb.s_full[i], 1);
         mbar_init(&tb.s_free[i], kSoftmaxThreads);
         mbar_init(&tb.p_full[i], kSoftmaxThreads);
+        mbar_init(&tb.p_free[i], 1);
       }
-      mbar_init(tb.o_done, 1);
     }
     fence_mbar_init();
   }
@@ -254,16 +263,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- producer: K/V tiles of four blocks each
     const int32_t* table = p.block_tables + (long long)n * p.max_blocks_per_seq + first;
     const int nblk = last - first + 1;
+    // block ids, 32 at a time: lane l holds entry 32*k + l of batch k; batch k+1
+    // is loaded while batch k is used, so the table's latency stays off the path
+    constexpr int kTilesPerBatch = 32 / kTileBlocks;
+    auto batch = [&](int k) { return 32 * k + lane < nblk ? table[32 * k + lane] : -1; };
+    int ids = batch(0), ids_next = batch(1);
     int issued = 0;
     for (int t = 0; t < ntiles && !timed_out; t++, issued++) {
       const int st = t % kNS;
+      if (t > 0 && t % kTilesPerBatch == 0) {
+        ids = ids_next;
+        ids_next = batch(t / kTilesPerBatch + 1);
+      }
+      const int from = __shfl_sync(0xffffffffu, ids, (kTileBlocks * t + lane) & 31);
+      const bool inside = lane < kTileBlocks && kTileBlocks * t + lane < nblk;
+      const int mine = inside ? from : -1;
+      const bool ok = inside && mine >= 0 && mine < p.num_blocks;
       if (t >= kNS && !mbar_wait(&kv_free[st], ((t / kNS) - 1) & 1)) {
         timed_out = true;
         break;
       }
-      const bool inside = lane < kTileBlocks && kTileBlocks * t + lane < nblk;
-      const int mine = inside ? table[kTileBlocks * t + lane] : -1;
-      const bool ok = inside && mine >= 0 && mine < p.num_blocks;
       if (lane < kTileBlocks) {
         vflags[st * kTileBlocks + lane] = ok ? 1 : 0;
         if (inside && !ok) set_flag(p.err, PA_FLAG_BLOCK_ID);
@@ -293,13 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&kv_full[t % kNS], (t / kNS) & 1)) break;
     if (timed_out && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
   } else if (warp == 1) {
-    // ---------------- MMA issuer (one thread)
-    if (lane == 0) {
+    // ---------------- MMA issuer (the whole warp; one elected lane issues)
+    {
       const uint32_t idS = idesc<BF>(kRows, kKeys, false);
       const uint32_t idO = idesc<BF>(kRows, D, true);
       auto pv = [&](int q, int t) -> bool {  // O_q += P_{q,t} V_t
         const TileBars tb = tile_bars(tbar0 + q * LY::kTileBars);
-        if (!mbar_wait(&tb.p_full[t & 1], (t >> 1) & 1)) return false;
+        if (!warp_wait(&tb.p_full[t & 1], (t >> 1) & 1)) return false;
         fence_after();
         const uint32_t sP = smem_u32(smem + LY::kPOff + (2 * q + (t & 1)) * LY::kPBytes);
         const uint32_t sV = smem_u32(smem + LY::kStageOff + (t % kNS) * LY::kStageBytes) +
@@ -307,40 +326,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dO = tmem + q * LY::kTileCols + LY::kOCol;
 #pragma unroll
         for (int s = 0; s < kKeys / 16; s++)
-          mma(dO, sw128_desc(sP + 32 * s, 16, 1024),
-              sw128_desc(sV + 2048 * s, LY::kKVChunk, 1024), idO, (t > 0 || s > 0) ? 1u : 0u);
-        commit(tb.o_done);
+          mma_elect(dO, sw128_desc(sP + 32 * s, 16, 1024),
+                    sw128_desc(sV + 2048 * s, LY::kKVChunk, 1024), idO, (t > 0 || s > 0) ? 1u : 0u);
+        commit_elect(&tb.p_free[t & 1]);
         return true;
       };
-      bool ok = mbar_wait(q_full, 0);
+      bool ok = warp_wait(q_full, 0);
       for (int t = 0; t < ntiles && ok; t++) {
         const int st = t % kNS;
-        ok = mbar_wait(&kv_full[st], (t / kNS) & 1);
+        ok = warp_wait(&kv_full[st], (t / kNS) & 1);
         const uint32_t sK = smem_u32(smem + LY::kStageOff + st * LY::kStageBytes);
         for (int q = 0; q < kQTiles && ok; q++) {
           const TileBars tb = tile_bars(tbar0 + q * LY::kTileBars);
-          if (t >= 2) ok = mbar_wait(&tb.s_free[t & 1], ((t - 2) >> 1) & 1);
+          if (t >= 2) ok = warp_wait(&tb.s_free[t & 1], ((t - 2) >> 1) & 1);
           if (!ok) break;
           fence_after();
           const uint32_t sQ = smem_u32(smem + LY::kQOff + q * LY::kQBytes);
           const uint32_t dS = tmem + q * LY::kTileCols + ((t & 1) ? LY::kSCol1 : LY::kSCol0);
 #pragma unroll
           for (int s = 0; s < D / 16; s++)
-            mma(dS, sw128_desc(sQ + (s / 4) * (kRows * 128) + (s % 4) * 32, 16, 1024),
-                sw128_desc(sK + (s / 4) * LY::kKVChunk + (s % 4) * 32, 16, 1024), idS,
-                s > 0 ? 1u : 0u);
-          commit(&tb.s_full[t & 1]);
+            mma_elect(dS, sw128_desc(sQ + (s / 4) * (kRows * 128) + (s % 4) * 32, 16, 1024),
+                      sw128_desc(sK + (s / 4) * LY::kKVChunk + (s % 4) * 32, 16, 1024), idS,
+                      s > 0 ? 1u : 0u);
+          commit_elect(&tb.s_full[t & 1]);
         }
         if (ok && t >= 1) {
           for (int q = 0; q < kQTiles && ok; q++) ok = pv(q, t - 1);
-          if (ok) commit(&kv_free[(t - 1) % kNS]);
+          if (ok) commit_elect(&kv_free[(t - 1) % kNS]);
         }
       }
       if (ok) {
         for (int q = 0; q < kQTiles && ok; q++) ok = pv(q, ntiles - 1);
-        if (ok) commit(&kv_free[(ntiles - 1) % kNS]);
+        if (ok) commit_elect(&kv_free[(ntiles - 1) % kNS]);
       }
-      if (!ok) set_flag(p.err, PA_FLAG_TIMEOUT);
+      if (!ok && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
     }
     __syncwarp();
   } else {
@@ -372,11 +391,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(q_full);
     }
 
-    // o_done completes once per P V of this tile.  It is waited on at every key
-    // tile t >= 1 (for the P V of tile t-1): early when O must be rescaled,
-    // otherwise just before P is written; waiting again on that same, completed
-    // phase returns at once, and the barrier cannot move on before this tile's
-    // P is published.
+    // p_free[b] completes when the P V that read P buffer b has finished, and
+    // with it every earlier MMA.  Tile t waits on it for the P V of tile t-1
+    // (buffer (t-1)&1) before rescaling O, and for the P V of tile t-2 (buffer
+    // t&1) before writing P.  Per buffer these are successive phases, and a
+    // repeated wait on the same phase is safe: the next one needs this tile's P.
     float m_used = kNoMax, l = 0.0f;
     for (int t = 0; t < ntiles; t++) {
       if (!mbar_wait(&tb.s_full[t & 1], (t >> 1) & 1)) {
@@ -432,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_new = need ? mt : m_used;
         const float factor = need ? fast_exp2(m_used - m_new) : 1.0f;
         if (t > 0) {  // O holds tiles < t: wait for the last P V, then scale it in place
-          if (!mbar_wait(tb.o_done, (t - 1) & 1)) {
+          if (!mbar_wait(&tb.p_free[(t - 1) & 1], ((t - 1) >> 1) & 1)) {
             timed_out = true;
             break;
           }
@@ -461,9 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         part[i & 7] += x[i];
       }
       l += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
-      // the P V of tile t-1 has finished: O is settled, and P buffer t&1 (last
-      // read by the P V of tile t-2) is free
-      if (t > 0 && !mbar_wait(tb.o_done, (t - 1) & 1)) {
+      // P buffer t&1 was last read by the P V of tile t-2
+      if (t >= 2 && !mbar_wait(&tb.p_free[t & 1], ((t - 2) >> 1) & 1)) {
         timed_out = true;
         break;
       }
@@ -498,8 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_before();
       mbar_arrive(&tb.p_full[t & 1]);
     }
-    // epilogue: wait for the last P V (its predecessor was waited at the last tile)
-    if (!timed_out && mbar_wait(tb.o_done, (ntiles - 1) & 1)) {
+    // epilogue: wait for the last P V
+    if (!timed_out && mbar_wait(&tb.p_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) {
       fence_after();
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
       QT* dst = out + orow * D;
