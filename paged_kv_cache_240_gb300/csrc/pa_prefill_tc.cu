@@ -22,6 +22,8 @@
 // before, so every barrier is waited on at every phase, in order; every wait is
 // bounded.
 #include <algorithm>
+#include <cstring>
+#include <type_traits>
 
 #include "pa_attn_common.cuh"
 #include "pa_internal.h"
@@ -39,6 +41,8 @@ constexpr int kSoftmaxThreads = 128;  // per query tile
 constexpr int kThreads = 64 + kQTiles * kSoftmaxThreads;  // 10 warps
 constexpr float kLazyRescale = 8.0f;  // log2 of the growth that forces a rescale
 constexpr float kNoMax = -1.0e30f;    // running-maximum sentinel: 2^(-inf - kNoMax) = 0
+constexpr int kMaxPlan = 512;         // (sequence, tile) pairs the CTA orders by cost
+constexpr int kItemCost = 2;          // per-item overhead, in key tiles
 
 template <int D>
 struct Layout {
@@ -52,13 +56,14 @@ struct Layout {
   static constexpr int kStageOff = kQOff + kQTiles * kQBytes;
   static constexpr int kPOff = kStageOff + kNS * kStageBytes;  // [tile][buffer]
   static constexpr int kBarOff = kPOff + kQTiles * 2 * kPBytes;
-  // barriers: kv_full[NS], kv_free[NS], q_full, then per query tile s_full[2],
-  // s_free[2], p_full[2], p_free[2]
+  // barriers: kv_full[NS], kv_free[NS], q_full, q_free, then per query tile
+  // s_full[2], s_free[2], p_full[2], p_free[2]
   static constexpr int kTileBars = 8;
-  static constexpr int kNumBars = 2 * kNS + 1 + kQTiles * kTileBars;
+  static constexpr int kNumBars = 2 * kNS + 2 + kQTiles * kTileBars;
   static constexpr int kFlagOff = kBarOff + kNumBars * 8;  // valid flags [NS][4] ints
   static constexpr int kTmemSlotOff = kFlagOff + kNS * kTileBlocks * 4;
-  static constexpr int kUsed = kTmemSlotOff + 16;
+  static constexpr int kOrderOff = kTmemSlotOff + 16;  // work order [kMaxPlan] uint16
+  static constexpr int kUsed = kOrderOff + kMaxPlan * 2;
   static constexpr int kBytes = kUsed + 1024;  // room to align the base to 1024
   // tensor memory columns per query tile: S buffers 0/1, then O
   static constexpr uint32_t kSCol0 = 0, kSCol1 = kKeys, kOCol = 2 * kKeys;
@@ -173,11 +178,89 @@ __device__ __forceinline__ uint32_t sw_unit(int r, int u) {
   return (uint32_t)(r * 128 + (((u ^ r) & 7) << 4));
 }
 
+// One work item: 256 query rows (two tiles) of one sequence's chunk and one kv
+// head, and the key range those rows can see.
+struct Item {
+  bool valid;  // rows exist (a sequence whose chunk is shorter has fewer items)
+  int n, kvh, q0, C, L, R0, nrows, lo_u, hi_u, first, ntiles;
+};
+
+__device__ __forceinline__ Item item_info(const AttnParams& p, int n, int kvh, int tile,
+                                          bool report) {
+  Item it;
+  it.valid = false;
+  it.ntiles = 0;
+  it.n = n;
+  it.kvh = kvh;
+  report = report && kvh == 0 && tile == 0;  // one report per sequence
+  const int q0 = p.cu_q_lens[it.n], q1 = p.cu_q_lens[it.n + 1];
+  if (q0 < 0 || q1 < q0 || q1 > p.num_q_tokens) {
+    if (report) set_flag(p.err, PA_FLAG_Q_LEN);
+    return it;
+  }
+  int C = q1 - q0;
+  if (C > p.max_q_len) {
+    if (report) set_flag(p.err, PA_FLAG_Q_LEN);
+    C = p.max_q_len;
+  }
+  const int L = clamp_context(p, it.n, report);
+  if (C > L && report) set_flag(p.err, PA_FLAG_Q_LEN);
+  it.q0 = q0;
+  it.C = C;
+  it.L = L;
+  it.R0 = tile * kCtaRows;
+  it.nrows = C * p.group;
+  if (it.R0 >= it.nrows) return it;
+  it.valid = true;
+  const int c_first = it.R0 / p.group;
+  const int c_last = (min(it.R0 + kCtaRows, it.nrows) - 1) / p.group;
+  it.hi_u = L - C + c_last;
+  it.lo_u = p.window > 0 ? max(0, L - C + c_first - p.window + 1) : 0;
+  it.first = it.lo_u / kBlock;
+  const int last = it.hi_u / kBlock;
+  it.ntiles = it.hi_u >= it.lo_u ? (last - it.first) / kTileBlocks + 1 : 0;
+  return it;
+}
+
+// The work list: items ordered by cost (key tiles + a fixed overhead), longest
+// first, when the CTA could rank the (sequence, tile) pairs (every kv head of a
+// pair costs the same); in (sequence, kv head, tile) order otherwise.  Round r
+// of the list goes to the CTAs in alternating directions (CTA b takes position
+// r*grid + b in even rounds, r*grid + grid-1-b in odd ones), so a CTA that drew
+// a long item early draws a short one next.  Returns false past the end.
+struct WorkList {
+  const uint16_t* order;  // pair index by rank, or nullptr
+  int num_pairs, kv_heads, q_tiles;
+
+  __device__ __forceinline__ bool at(int j, int& n, int& kvh, int& tile) const {
+    const int grid = gridDim.x, b = blockIdx.x;
+    const long long s = (long long)j * grid + ((j & 1) ? grid - 1 - b : b);
+    if (s >= (long long)num_pairs * kv_heads) return false;
+    if (order) {
+      const int pair = order[s / kv_heads];
+      kvh = (int)(s % kv_heads);
+      n = pair / q_tiles;
+      tile = pair % q_tiles;
+    } else {
+      const int per_seq = q_tiles * kv_heads;
+      n = (int)(s / per_seq);
+      kvh = (int)(s % per_seq) / q_tiles;
+      tile = (int)(s % per_seq) % q_tiles;
+    }
+    return true;
+  }
+};
+
+// Persistent: each CTA walks its part of the work list.  Every role walks the
+// same items; the tile counter g (and the item counter k for Q) runs on across
+// items, so each barrier keeps stepping one phase at a time, and the next
+// item's Q and first K/V tiles load while the current item's last tiles finish.
 template <int D, typename QT>
 __global__ void __launch_bounds__(kThreads, 1)
     pa_prefill_tc_kernel(const __grid_constant__ AttnParams p,
                          const __grid_constant__ CUtensorMap tmk,
-                         const __grid_constant__ CUtensorMap tmv) {
+                         const __grid_constant__ CUtensorMap tmv,
+                         const __grid_constant__ CUtensorMap tmq, int num_seqs, int q_tma) {
   using LY = Layout<D>;
   constexpr bool BF = std::is_same<QT, __nv_bfloat16>::value;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -186,56 +269,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_full = bars;
   uint64_t* kv_free = bars + kNS;
   uint64_t* q_full = bars + 2 * kNS;
-  uint64_t* tbar0 = q_full + 1;  // per-tile barriers follow
+  uint64_t* q_free = q_full + 1;
+  uint64_t* tbar0 = q_full + 2;  // per-tile barriers follow
   int* vflags = reinterpret_cast<int*>(smem + LY::kFlagOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::kTmemSlotOff);
 
-  const int n = blockIdx.y;
-  const int tile = blockIdx.x % p.q_tiles;
-  const int kvh = blockIdx.x / p.q_tiles;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
-  const bool reporter = threadIdx.x == 0 && blockIdx.x == 0;
-
-  const int q0 = p.cu_q_lens[n], q1 = p.cu_q_lens[n + 1];
-  if (q0 < 0 || q1 < q0 || q1 > p.num_q_tokens) {
-    if (reporter) set_flag(p.err, PA_FLAG_Q_LEN);
-    return;
-  }
-  int C = q1 - q0;
-  if (C > p.max_q_len) {
-    if (reporter) set_flag(p.err, PA_FLAG_Q_LEN);
-    C = p.max_q_len;
-  }
-  const int L = clamp_context(p, n, reporter);
-  if (C > L && reporter) set_flag(p.err, PA_FLAG_Q_LEN);
-  const int R0 = tile * kCtaRows;
-  const int nrows = C * G;
-  if (R0 >= nrows) return;
-  const int c_first = R0 / G;
-  const int c_last = (min(R0 + kCtaRows, nrows) - 1) / G;
-  const int hi_u = L - C + c_last;
-  const int lo_u = p.window > 0 ? max(0, L - C + c_first - p.window + 1) : 0;
-  const int first = lo_u / kBlock;
-  const int last = hi_u / kBlock;
-  const int ntiles = hi_u >= lo_u ? (last - first) / kTileBlocks + 1 : 0;
-  QT* out = static_cast<QT*>(p.out);
-  if (ntiles == 0) {  // no row sees a key: zeros
-    for (int idx = threadIdx.x; idx < kCtaRows * D; idx += kThreads) {
-      const int R = R0 + idx / D;
-      if (R < nrows)
-        out[((long long)(q0 + R / G) * p.num_q_heads + kvh * G + R % G) * D + idx % D] =
-            to_out<QT>(0.0f);
-    }
-    return;
-  }
+  const bool reporter = threadIdx.x == 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNS; i++) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_free[i], 1);
     }
-    mbar_init(q_full, kQTiles * kSoftmaxThreads);
+    mbar_init(q_full, 32);  // the producer warp's lanes
+    mbar_init(q_free, 1);
     for (int q = 0; q < kQTiles; q++) {
       const TileBars tb = tile_bars(tbar0 + q * LY::kTileBars);
       for (int i = 0; i < 2; i++) {
@@ -253,6 +302,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                  "r"(LY::kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  // the work order (the P buffers serve as scratch: nothing has written them yet)
+  WorkList wl;
+  wl.num_pairs = num_seqs * p.q_tiles;
+  wl.kv_heads = p.num_kv_heads;
+  wl.q_tiles = p.q_tiles;
+  wl.order = nullptr;
+  if (wl.num_pairs <= kMaxPlan) {
+    int* cost = reinterpret_cast<int*>(smem + LY::kPOff);
+    uint16_t* order = reinterpret_cast<uint16_t*>(smem + LY::kOrderOff);
+    for (int j = threadIdx.x; j < wl.num_pairs; j += kThreads) {
+      const Item it = item_info(p, j / p.q_tiles, 0, j % p.q_tiles, false);
+      cost[j] = it.valid ? it.ntiles + kItemCost : 0;
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < wl.num_pairs; j += kThreads) {
+      const int cj = cost[j];
+      int rank = 0;
+      for (int i2 = 0; i2 < wl.num_pairs; i2++) {
+        const int ci = cost[i2];
+        rank += (ci > cj || (ci == cj && i2 < j)) ? 1 : 0;
+      }
+      order[rank] = (uint16_t)j;
+    }
+    wl.order = order;
+  }
   fence_before();
   __syncthreads();
   fence_after();
@@ -260,107 +334,159 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool timed_out = false;
 
   if (warp == 0) {
-    // ---------------- producer: K/V tiles of four blocks each
-    const int32_t* table = p.block_tables + (long long)n * p.max_blocks_per_seq + first;
-    const int nblk = last - first + 1;
-    // block ids, 32 at a time: lane l holds entry 32*k + l of batch k; batch k+1
-    // is loaded while batch k is used, so the table's latency stays off the path
-    constexpr int kTilesPerBatch = 32 / kTileBlocks;
-    auto batch = [&](int k) { return 32 * k + lane < nblk ? table[32 * k + lane] : -1; };
-    int ids = batch(0), ids_next = batch(1);
-    int issued = 0;
-    for (int t = 0; t < ntiles && !timed_out; t++, issued++) {
-      const int st = t % kNS;
-      if (t > 0 && t % kTilesPerBatch == 0) {
-        ids = ids_next;
-        ids_next = batch(t / kTilesPerBatch + 1);
-      }
-      const int from = __shfl_sync(0xffffffffu, ids, (kTileBlocks * t + lane) & 31);
-      const bool inside = lane < kTileBlocks && kTileBlocks * t + lane < nblk;
-      const int mine = inside ? from : -1;
-      const bool ok = inside && mine >= 0 && mine < p.num_blocks;
-      if (t >= kNS && !mbar_wait(&kv_free[st], ((t / kNS) - 1) & 1)) {
+    // ---------------- producer: each item's Q, then its K/V tiles of four blocks
+    int g = 0, k = 0;  // tiles and items with tiles so far
+    int n, kvh, tile;
+    for (int j = 0; !timed_out && wl.at(j, n, kvh, tile); j++) {
+      const Item it = item_info(p, n, kvh, tile, reporter);
+      if (!it.valid || it.ntiles == 0) continue;
+      // Q of this item, once the previous item's S MMAs have finished with it
+      if (k > 0 && !warp_wait(q_free, (k - 1) & 1)) {
         timed_out = true;
         break;
       }
-      if (lane < kTileBlocks) {
-        vflags[st * kTileBlocks + lane] = ok ? 1 : 0;
-        if (inside && !ok) set_flag(p.err, PA_FLAG_BLOCK_ID);
-      }
-      __syncwarp();  // every lane's flag is written before lane 0 arms the stage
-      const unsigned okmask = __ballot_sync(0xffffffffu, ok);
-      if (lane == 0)
-        mbar_arrive_expect_tx(&kv_full[st], __popc(okmask) * 2u * LY::kKVBytes / kTileBlocks);
-      __syncwarp();
-      if (ok) {
-        uint8_t* kbase = smem + LY::kStageOff + st * LY::kStageBytes;
-        uint8_t* vbase = kbase + LY::kKVBytes;
-        const int row0 = (mine * p.num_kv_heads + kvh) * kBlock;
+      uint8_t* qs = smem + LY::kQOff;
+      if (q_tma) {
+        // box [128/G tokens][G heads][64 columns] = 128 rows of the tile
+        if (lane == 0) mbar_arrive_expect_tx(q_full, kQTiles * LY::kQBytes);
+        __syncwarp();
+        if (lane < kQTiles * LY::kChunks) {
+          const int q = lane / LY::kChunks, h = lane % LY::kChunks;
+          tma_load_3d(qs + q * LY::kQBytes + h * (kRows * 128), &tmq, 64 * h, it.kvh * G,
+                      it.q0 + (it.R0 + q * kRows) / G, q_full);
+        }
+        if (lane != 0) mbar_arrive(q_full);
+      } else {
+        const QT* qg = static_cast<const QT*>(p.q);
+        for (int r = lane; r < kCtaRows; r += 32) {
+          const int R = it.R0 + r;
+          const bool rv = R < it.nrows;
+          const long long orow =
+              rv ? (long long)(it.q0 + R / G) * p.num_q_heads + it.kvh * G + R % G : 0;
+          const uint4* src = reinterpret_cast<const uint4*>(qg + orow * D);
+          uint8_t* qt = qs + (r / kRows) * LY::kQBytes;
 #pragma unroll
-        for (int h = 0; h < LY::kChunks; h++) {
-          tma_load_2d(kbase + h * LY::kKVChunk + lane * kBlock * 128, &tmk, 64 * h, row0,
-                      &kv_full[st]);
-          tma_load_2d(vbase + h * LY::kKVChunk + lane * kBlock * 128, &tmv, 64 * h, row0,
-                      &kv_full[st]);
+          for (int u = 0; u < D / 8; u++)
+            cp_async_16_or_zero(qt + (u / 8) * (kRows * 128) + sw_unit(r % kRows, u % 8), src + u,
+                                rv);
+        }
+        cp_async_wait_all();
+        fence_proxy_async();
+        mbar_arrive(q_full);
+      }
+      k++;
+      // K/V tiles; block ids 32 at a time (lane l holds entry 32*b + l of batch
+      // b), the next batch loaded while this one is used
+      const int32_t* table =
+          p.block_tables + (long long)it.n * p.max_blocks_per_seq + it.first;
+      const int nblk = it.hi_u / kBlock - it.first + 1;
+      constexpr int kTilesPerBatch = 32 / kTileBlocks;
+      auto batch = [&](int b) { return 32 * b + lane < nblk ? table[32 * b + lane] : -1; };
+      int ids = batch(0), ids_next = batch(1);
+      for (int t = 0; t < it.ntiles; t++, g++) {
+        const int st = g % kNS;
+        if (t > 0 && t % kTilesPerBatch == 0) {
+          ids = ids_next;
+          ids_next = batch(t / kTilesPerBatch + 1);
+        }
+        const int from = __shfl_sync(0xffffffffu, ids, (kTileBlocks * t + lane) & 31);
+        const bool inside = lane < kTileBlocks && kTileBlocks * t + lane < nblk;
+        const int mine = inside ? from : -1;
+        const bool ok = inside && mine >= 0 && mine < p.num_blocks;
+        if (g >= kNS && !warp_wait(&kv_free[st], ((g / kNS) - 1) & 1)) {
+          timed_out = true;
+          break;
+        }
+        if (lane < kTileBlocks) {
+          vflags[st * kTileBlocks + lane] = ok ? 1 : 0;
+          if (inside && !ok) set_flag(p.err, PA_FLAG_BLOCK_ID);
+        }
+        __syncwarp();  // every lane's flag is written before lane 0 arms the stage
+        const unsigned okmask = __ballot_sync(0xffffffffu, ok);
+        if (lane == 0)
+          mbar_arrive_expect_tx(&kv_full[st], __popc(okmask) * 2u * LY::kKVBytes / kTileBlocks);
+        __syncwarp();
+        if (ok) {
+          uint8_t* kbase = smem + LY::kStageOff + st * LY::kStageBytes;
+          uint8_t* vbase = kbase + LY::kKVBytes;
+          const int row0 = (mine * p.num_kv_heads + it.kvh) * kBlock;
+#pragma unroll
+          for (int h = 0; h < LY::kChunks; h++) {
+            tma_load_2d(kbase + h * LY::kKVChunk + lane * kBlock * 128, &tmk, 64 * h, row0,
+                        &kv_full[st]);
+            tma_load_2d(vbase + h * LY::kKVChunk + lane * kBlock * 128, &tmv, 64 * h, row0,
+                        &kv_full[st]);
+          }
         }
       }
     }
     // no copy may still be landing in shared memory when the CTA exits; the last
-    // kNS tiles issued are their stages' current phases
-    if (lane == 0)
-      for (int t = issued > kNS ? issued - kNS : 0; t < issued; t++)
+    // kNS tiles issued and the last Q are their barriers' current phases
+    if (lane == 0) {
+      for (int t = g > kNS ? g - kNS : 0; t < g; t++)
         if (!mbar_wait(&kv_full[t % kNS], (t / kNS) & 1)) break;
+      if (k > 0) mbar_wait(q_full, (k - 1) & 1);
+    }
     if (timed_out && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
   } else if (warp == 1) {
     // ---------------- MMA issuer (the whole warp; one elected lane issues)
-    {
-      const uint32_t idS = idesc<BF>(kRows, kKeys, false);
-      const uint32_t idO = idesc<BF>(kRows, D, true);
-      auto pv = [&](int q, int t) -> bool {  // O_q += P_{q,t} V_t
-        const TileBars tb = tile_bars(tbar0 + q * LY::kTileBars);
-        if (!warp_wait(&tb.p_full[t & 1], (t >> 1) & 1)) return false;
-        fence_after();
-        const uint32_t sP = smem_u32(smem + LY::kPOff + (2 * q + (t & 1)) * LY::kPBytes);
-        const uint32_t sV = smem_u32(smem + LY::kStageOff + (t % kNS) * LY::kStageBytes) +
-                            LY::kKVBytes;
-        const uint32_t dO = tmem + q * LY::kTileCols + LY::kOCol;
+    const uint32_t idS = idesc<BF>(kRows, kKeys, false);
+    const uint32_t idO = idesc<BF>(kRows, D, true);
+    // O_q (+)= P_{q,g} V_g; `first` starts a new accumulation
+    auto pv = [&](int q, int g, bool first) -> bool {
+      const TileBars tb = tile_bars(tbar0 + q * LY::kTileBars);
+      if (!warp_wait(&tb.p_full[g & 1], (g >> 1) & 1)) return false;
+      fence_after();
+      const uint32_t sP = smem_u32(smem + LY::kPOff + (2 * q + (g & 1)) * LY::kPBytes);
+      const uint32_t sV =
+          smem_u32(smem + LY::kStageOff + (g % kNS) * LY::kStageBytes) + LY::kKVBytes;
+      const uint32_t dO = tmem + q * LY::kTileCols + LY::kOCol;
 #pragma unroll
-        for (int s = 0; s < kKeys / 16; s++)
-          mma_elect(dO, sw128_desc(sP + 32 * s, 16, 1024),
-                    sw128_desc(sV + 2048 * s, LY::kKVChunk, 1024), idO, (t > 0 || s > 0) ? 1u : 0u);
-        commit_elect(&tb.p_free[t & 1]);
-        return true;
-      };
-      bool ok = warp_wait(q_full, 0);
-      for (int t = 0; t < ntiles && ok; t++) {
-        const int st = t % kNS;
-        ok = warp_wait(&kv_full[st], (t / kNS) & 1);
+      for (int s = 0; s < kKeys / 16; s++)
+        mma_elect(dO, sw128_desc(sP + 32 * s, 16, 1024),
+                  sw128_desc(sV + 2048 * s, LY::kKVChunk, 1024), idO,
+                  (!first || s > 0) ? 1u : 0u);
+      commit_elect(&tb.p_free[g & 1]);
+      return true;
+    };
+    bool ok = true;
+    int g = 0, k = 0;
+    int n, kvh, tile;
+    for (int j = 0; ok && wl.at(j, n, kvh, tile); j++) {
+      const Item it = item_info(p, n, kvh, tile, false);
+      if (!it.valid || it.ntiles == 0) continue;
+      ok = warp_wait(q_full, k & 1);
+      k++;
+      for (int t = 0; t < it.ntiles && ok; t++, g++) {
+        const int st = g % kNS;
+        ok = warp_wait(&kv_full[st], (g / kNS) & 1);
         const uint32_t sK = smem_u32(smem + LY::kStageOff + st * LY::kStageBytes);
         for (int q = 0; q < kQTiles && ok; q++) {
           const TileBars tb = tile_bars(tbar0 + q * LY::kTileBars);
-          if (t >= 2) ok = warp_wait(&tb.s_free[t & 1], ((t - 2) >> 1) & 1);
+          if (g >= 2) ok = warp_wait(&tb.s_free[g & 1], ((g - 2) >> 1) & 1);
           if (!ok) break;
           fence_after();
           const uint32_t sQ = smem_u32(smem + LY::kQOff + q * LY::kQBytes);
-          const uint32_t dS = tmem + q * LY::kTileCols + ((t & 1) ? LY::kSCol1 : LY::kSCol0);
+          const uint32_t dS = tmem + q * LY::kTileCols + ((g & 1) ? LY::kSCol1 : LY::kSCol0);
 #pragma unroll
           for (int s = 0; s < D / 16; s++)
             mma_elect(dS, sw128_desc(sQ + (s / 4) * (kRows * 128) + (s % 4) * 32, 16, 1024),
                       sw128_desc(sK + (s / 4) * LY::kKVChunk + (s % 4) * 32, 16, 1024), idS,
                       s > 0 ? 1u : 0u);
-          commit_elect(&tb.s_full[t & 1]);
+          commit_elect(&tb.s_full[g & 1]);
         }
+        if (ok && t == it.ntiles - 1) commit_elect(q_free);  // Q is no longer read
         if (ok && t >= 1) {
-          for (int q = 0; q < kQTiles && ok; q++) ok = pv(q, t - 1);
-          if (ok) commit_elect(&kv_free[(t - 1) % kNS]);
+          for (int q = 0; q < kQTiles && ok; q++) ok = pv(q, g - 1, t == 1);
+          if (ok) commit_elect(&kv_free[(g - 1) % kNS]);
         }
       }
       if (ok) {
-        for (int q = 0; q < kQTiles && ok; q++) ok = pv(q, ntiles - 1);
-        if (ok) commit_elect(&kv_free[(ntiles - 1) % kNS]);
+        for (int q = 0; q < kQTiles && ok; q++) ok = pv(q, g - 1, it.ntiles == 1);
+        if (ok) commit_elect(&kv_free[(g - 1) % kNS]);
       }
-      if (!ok && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
     }
+    if (!ok && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
     __syncwarp();
   } else {
     // ---------------- softmax: query tile q, thread <-> row (TMEM lane 32*(warp%4) + lane)
@@ -368,159 +494,163 @@ __global__ void __launch_bounds__(kThreads, 1)
     const TileBars tb = tile_bars(tbar0 + q * LY::kTileBars);
     const int stid = threadIdx.x - 64 - q * kSoftmaxThreads;  // 0..127 within the tile
     const int row = 32 * (warp & 3) + lane;
-    const int R = R0 + q * kRows + row;
-    const bool rvalid = R < nrows;
-    const int c = rvalid ? R / G : 0;
-    const int pos = L - C + c;
-    const int row_hi = rvalid ? pos : -1;
-    const int row_lo = p.window > 0 ? max(0, pos - p.window + 1) : 0;
-    const long long orow = (long long)(q0 + c) * p.num_q_heads + kvh * G + (rvalid ? R % G : 0);
     const uint32_t lane_base = tmem + q * LY::kTileCols + ((uint32_t)(32 * (warp & 3)) << 16);
     const float sc = p.scale_log2;
-
-    // Q row -> shared memory in the MMA's swizzled K-major layout
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const QT*>(p.q) + orow * D);
-      uint8_t* qt = smem + LY::kQOff + q * LY::kQBytes;
+    QT* out = static_cast<QT*>(p.out);
+    int g = 0;
+    int n, kvh, tile;
+    for (int j = 0; !timed_out && wl.at(j, n, kvh, tile); j++) {
+      const Item it = item_info(p, n, kvh, tile, false);
+      if (!it.valid) continue;
+      const int R = it.R0 + q * kRows + row;
+      const bool rvalid = R < it.nrows;
+      const int c = rvalid ? R / G : 0;
+      const int pos = it.L - it.C + c;
+      const int row_hi = rvalid ? pos : -1;
+      const int row_lo = p.window > 0 ? max(0, pos - p.window + 1) : 0;
+      const long long orow =
+          (long long)(it.q0 + c) * p.num_q_heads + it.kvh * G + (rvalid ? R % G : 0);
+      QT* dst = out + orow * D;
+      if (it.ntiles == 0) {  // no row sees a key: zeros
+        if (rvalid)
 #pragma unroll
-      for (int u = 0; u < D / 8; u++) {
-        const uint4 v = rvalid ? src[u] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(qt + (u / 8) * (kRows * 128) + sw_unit(row, u % 8)) = v;
+          for (int u = 0; u < D / 8; u++) reinterpret_cast<uint4*>(dst)[u] = make_uint4(0, 0, 0, 0);
+        continue;
       }
-      fence_proxy_async();
-      mbar_arrive(q_full);
-    }
-
-    // p_free[b] completes when the P V that read P buffer b has finished, and
-    // with it every earlier MMA.  Tile t waits on it for the P V of tile t-1
-    // (buffer (t-1)&1) before rescaling O, and for the P V of tile t-2 (buffer
-    // t&1) before writing P.  Per buffer these are successive phases, and a
-    // repeated wait on the same phase is safe: the next one needs this tile's P.
-    float m_used = kNoMax, l = 0.0f;
-    for (int t = 0; t < ntiles; t++) {
-      if (!mbar_wait(&tb.s_full[t & 1], (t >> 1) & 1)) {
+      // p_free[b] completes when the P V that read P buffer b has finished, and
+      // with it every earlier MMA.  Tile g waits on it for the P V of tile g-1
+      // (buffer (g-1)&1) before rescaling O, and for the P V of tile g-2 (buffer
+      // g&1) before writing P.  Per buffer these are successive phases, and a
+      // repeated wait on the same phase is safe: the next one needs this tile's P.
+      float m_used = kNoMax, l = 0.0f;
+      for (int t = 0; t < it.ntiles; t++, g++) {
+        if (!mbar_wait(&tb.s_full[g & 1], (g >> 1) & 1)) {
+          timed_out = true;
+          break;
+        }
+        fence_after();
+        const int pos0 = (it.first + kTileBlocks * t) * kBlock;
+        const int* vf = vflags + (g % kNS) * kTileBlocks;
+        const bool blocks_ok = vf[0] && vf[1] && vf[2] && vf[3];
+        float x[kKeys];
+        {
+          float v[32];
+          const uint32_t scol = (g & 1) ? LY::kSCol1 : LY::kSCol0;
+          tmem_ld32(lane_base + scol, v);
+#pragma unroll
+          for (int j = 0; j < 32; j++) x[j] = v[j];
+          tmem_ld32(lane_base + scol + 32, v);
+#pragma unroll
+          for (int j = 0; j < 32; j++) x[32 + j] = v[j];
+        }
+        fence_before();
+        mbar_arrive(&tb.s_free[g & 1]);  // the MMA may overwrite this S buffer now
+        // maximum of the scaled scores this row can see; an inner tile (every key
+        // visible to every row of the warp) skips the masks.  Eight partial maxima
+        // and sums keep the dependency chains short.
+        float part[8];
+        const bool inner = __all_sync(0xffffffffu, blocks_ok && pos0 >= row_lo &&
+                                                       pos0 + kKeys - 1 <= row_hi) &&
+                           sc > 0.0f;
+        if (inner) {
+#pragma unroll
+          for (int j = 0; j < 8; j++) part[j] = x[j];
+#pragma unroll
+          for (int j = 8; j < kKeys; j++) part[j & 7] = fmaxf(part[j & 7], x[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; j++) part[j] = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < kKeys; j++) {
+            const int kp = pos0 + j;
+            const bool vis = kp >= row_lo && kp <= row_hi && vf[j / kBlock];
+            x[j] = vis ? x[j] * sc : -INFINITY;
+            part[j & 7] = fmaxf(part[j & 7], x[j]);
+          }
+        }
+        float mt = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
+                         fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
+        if (inner) mt *= sc;
+        // lazy rescale: only when this row's maximum grew by more than 2^8
+        const bool need = mt > m_used + kLazyRescale;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? mt : m_used;
+          const float factor = need ? fast_exp2(m_used - m_new) : 1.0f;
+          if (t > 0) {  // O holds this item's tiles < t: wait for the last P V, scale O
+            if (!mbar_wait(&tb.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1)) {
+              timed_out = true;
+              break;
+            }
+            fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              float v[32];
+              tmem_ld32(lane_base + LY::kOCol + c0, v);
+#pragma unroll
+              for (int j = 0; j < 32; j++) v[j] *= factor;
+              tmem_st32(lane_base + LY::kOCol + c0, v);
+            }
+          }
+          l *= factor;
+          m_used = m_new;
+        }
+        // inner tiles hold raw scores (the scale is folded into one FFMA), edge
+        // tiles already-scaled ones (-inf where masked)
+        const float mul = inner ? sc : 1.0f;
+        const float sub = -m_used;
+#pragma unroll
+        for (int j = 0; j < 8; j++) part[j] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kKeys; j++) {
+          x[j] = fast_exp2(fmaf(x[j], mul, sub));
+          part[j & 7] += x[j];
+        }
+        l += ((part[0] + part[1]) + (part[2] + part[3])) +
+             ((part[4] + part[5]) + (part[6] + part[7]));
+        // P buffer g&1 was last read by the P V of tile g-2
+        if (g >= 2 && !mbar_wait(&tb.p_free[g & 1], ((g - 2) >> 1) & 1)) {
+          timed_out = true;
+          break;
+        }
+        // P row -> shared memory (f16/bf16, K-major swizzled)
+        uint8_t* prow = smem + LY::kPOff + (2 * q + (g & 1)) * LY::kPBytes;
+#pragma unroll
+        for (int u = 0; u < kKeys / 8; u++) {
+          uint4 pk;
+          pk.x = pack2<BF>(x[8 * u + 0], x[8 * u + 1]);
+          pk.y = pack2<BF>(x[8 * u + 2], x[8 * u + 3]);
+          pk.z = pack2<BF>(x[8 * u + 4], x[8 * u + 5]);
+          pk.w = pack2<BF>(x[8 * u + 6], x[8 * u + 7]);
+          *reinterpret_cast<uint4*>(prow + sw_unit(row, u)) = pk;
+        }
+        // V rows of keys no row can see (before the window, past the context,
+        // blocks not in the pool) may hold garbage: zero them so 0 * V stays 0.
+        // Both query tiles read the stage; tile 0's warps clear it, and the MMA
+        // warp waits for tile 0's P before either tile's P V.
+        const bool edge = pos0 < it.lo_u || pos0 + kKeys - 1 > it.hi_u || !blocks_ok;
+        if (edge && q == 0) {
+          uint8_t* vbase = smem + LY::kStageOff + (g % kNS) * LY::kStageBytes + LY::kKVBytes;
+          for (int idx = stid; idx < kKeys * LY::kChunks * 8; idx += kSoftmaxThreads) {
+            const int key = idx / (LY::kChunks * 8);
+            const int rest = idx % (LY::kChunks * 8);
+            const int kp = pos0 + key;
+            if (kp < it.lo_u || kp > it.hi_u || !vf[key / kBlock])
+              *reinterpret_cast<uint4*>(vbase + (rest / 8) * LY::kKVChunk +
+                                        sw_unit(key, rest % 8)) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async();
+        fence_before();
+        mbar_arrive(&tb.p_full[g & 1]);
+      }
+      if (timed_out) break;
+      // epilogue: wait for this item's last P V (tile g-1)
+      if (!mbar_wait(&tb.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1)) {
         timed_out = true;
         break;
       }
-      fence_after();
-      const int pos0 = (first + kTileBlocks * t) * kBlock;
-      const int* vf = vflags + (t % kNS) * kTileBlocks;
-      const bool blocks_ok = vf[0] && vf[1] && vf[2] && vf[3];
-      float x[kKeys];
-      {
-        float v[32];
-        const uint32_t scol = (t & 1) ? LY::kSCol1 : LY::kSCol0;
-        tmem_ld32(lane_base + scol, v);
-#pragma unroll
-        for (int i = 0; i < 32; i++) x[i] = v[i];
-        tmem_ld32(lane_base + scol + 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; i++) x[32 + i] = v[i];
-      }
-      fence_before();
-      mbar_arrive(&tb.s_free[t & 1]);  // the MMA may overwrite this S buffer now
-      // maximum of the scaled scores this row can see; an inner tile (every key
-      // visible to every row of the warp) skips the masks.  Eight partial maxima
-      // and sums keep the dependency chains short.
-      float part[8];
-      const bool inner = __all_sync(0xffffffffu, blocks_ok && pos0 >= row_lo &&
-                                                     pos0 + kKeys - 1 <= row_hi) &&
-                         sc > 0.0f;
-      if (inner) {
-#pragma unroll
-        for (int j = 0; j < 8; j++) part[j] = x[j];
-#pragma unroll
-        for (int i = 8; i < kKeys; i++) part[i & 7] = fmaxf(part[i & 7], x[i]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; j++) part[j] = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kKeys; i++) {
-          const int kp = pos0 + i;
-          const bool vis = kp >= row_lo && kp <= row_hi && vf[i / kBlock];
-          x[i] = vis ? x[i] * sc : -INFINITY;
-          part[i & 7] = fmaxf(part[i & 7], x[i]);
-        }
-      }
-      float mt = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
-                       fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
-      if (inner) mt *= sc;
-      // lazy rescale: only when this row's maximum grew by more than 2^8
-      const bool need = mt > m_used + kLazyRescale;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? mt : m_used;
-        const float factor = need ? fast_exp2(m_used - m_new) : 1.0f;
-        if (t > 0) {  // O holds tiles < t: wait for the last P V, then scale it in place
-          if (!mbar_wait(&tb.p_free[(t - 1) & 1], ((t - 1) >> 1) & 1)) {
-            timed_out = true;
-            break;
-          }
-          fence_after();
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            float v[32];
-            tmem_ld32(lane_base + LY::kOCol + c0, v);
-#pragma unroll
-            for (int i = 0; i < 32; i++) v[i] *= factor;
-            tmem_st32(lane_base + LY::kOCol + c0, v);
-          }
-        }
-        l *= factor;
-        m_used = m_new;
-      }
-      // inner tiles hold raw scores (the scale is folded into one FFMA), edge
-      // tiles already-scaled ones (-inf where masked)
-      const float mul = inner ? sc : 1.0f;
-      const float sub = -m_used;
-#pragma unroll
-      for (int j = 0; j < 8; j++) part[j] = 0.0f;
-#pragma unroll
-      for (int i = 0; i < kKeys; i++) {
-        x[i] = fast_exp2(fmaf(x[i], mul, sub));
-        part[i & 7] += x[i];
-      }
-      l += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
-      // P buffer t&1 was last read by the P V of tile t-2
-      if (t >= 2 && !mbar_wait(&tb.p_free[t & 1], ((t - 2) >> 1) & 1)) {
-        timed_out = true;
-        break;
-      }
-      // P row -> shared memory (f16/bf16, K-major swizzled)
-      uint8_t* prow = smem + LY::kPOff + (2 * q + (t & 1)) * LY::kPBytes;
-#pragma unroll
-      for (int u = 0; u < kKeys / 8; u++) {
-        uint4 pk;
-        pk.x = pack2<BF>(x[8 * u + 0], x[8 * u + 1]);
-        pk.y = pack2<BF>(x[8 * u + 2], x[8 * u + 3]);
-        pk.z = pack2<BF>(x[8 * u + 4], x[8 * u + 5]);
-        pk.w = pack2<BF>(x[8 * u + 6], x[8 * u + 7]);
-        *reinterpret_cast<uint4*>(prow + sw_unit(row, u)) = pk;
-      }
-      // V rows of keys no row can see (before the window, past the context,
-      // blocks not in the pool) may hold garbage: zero them so 0 * V stays 0.
-      // Both query tiles read the stage; tile 0's warps clear it, and the MMA
-      // thread waits for tile 0's P before either tile's P V.
-      const bool edge = pos0 < lo_u || pos0 + kKeys - 1 > hi_u || !blocks_ok;
-      if (edge && q == 0) {
-        uint8_t* vbase = smem + LY::kStageOff + (t % kNS) * LY::kStageBytes + LY::kKVBytes;
-        for (int idx = stid; idx < kKeys * LY::kChunks * 8; idx += kSoftmaxThreads) {
-          const int key = idx / (LY::kChunks * 8);
-          const int rest = idx % (LY::kChunks * 8);
-          const int kp = pos0 + key;
-          if (kp < lo_u || kp > hi_u || !vf[key / kBlock])
-            *reinterpret_cast<uint4*>(vbase + (rest / 8) * LY::kKVChunk + sw_unit(key, rest % 8)) =
-                make_uint4(0, 0, 0, 0);
-        }
-      }
-      fence_proxy_async();
-      fence_before();
-      mbar_arrive(&tb.p_full[t & 1]);
-    }
-    // epilogue: wait for the last P V
-    if (!timed_out && mbar_wait(&tb.p_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) {
       fence_after();
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-      QT* dst = out + orow * D;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         float v[32];
@@ -537,8 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-    } else {
-      timed_out = true;
+      fence_before();  // O's reads are ordered before the next item's first P V
     }
     if (timed_out && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
   }
@@ -552,6 +681,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace tc
 
+namespace {
+
+int sm_count() {
+  static int count[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (count[dev] == 0 &&
+      cudaDeviceGetAttribute(&count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    count[dev] = 0;
+  return count[dev];
+}
+
+// Q as a 3-D tensor map [tokens][q heads][head_dim] whose box is one query tile:
+// 128/G tokens x G heads x 64 columns (128-byte swizzle).  Possible when G
+// divides 128 and the strides are multiples of 16 bytes.
+bool encode_q_map(CUtensorMap* m, const AttnParams& p, int D, bool bf16) {
+  if (tc::kRows % p.group != 0 || !pa_internal::aligned16(p.q)) return false;
+  pa_internal::EncodeTiledFn fn = pa_internal::encode_tiled_fn();
+  if (!fn || p.num_q_tokens <= 0) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.num_q_heads,
+                              (cuuint64_t)p.num_q_tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.num_q_heads * D * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)p.group, (cuuint32_t)(tc::kRows / p.group)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+            const_cast<void*>(p.q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 template <int D, typename QT>
 cudaError_t launch_prefill_tc(const AttnParams& p, const CUtensorMap& tmk,
                               const CUtensorMap& tmv, int num_seqs, cudaStream_t stream) {
@@ -561,8 +722,16 @@ cudaError_t launch_prefill_tc(const AttnParams& p, const CUtensorMap& tmk,
   if (e != cudaSuccess) return e;
   AttnParams pt = p;
   pt.q_tiles = (int)(((long long)p.max_q_len * p.group + tc::kCtaRows - 1) / tc::kCtaRows);
-  const dim3 grid((unsigned)(pt.q_tiles * pt.num_kv_heads), (unsigned)num_seqs);
-  kern<<<grid, tc::kThreads, smem, stream>>>(pt, tmk, tmv);
+  const long long items = (long long)pt.q_tiles * pt.num_kv_heads * num_seqs;
+  if (items <= 0) return cudaSuccess;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  CUtensorMap tmq;
+  memset(&tmq, 0, sizeof(tmq));
+  const bool q_tma = encode_q_map(&tmq, pt, D, std::is_same<QT, __nv_bfloat16>::value);
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const unsigned grid = (unsigned)std::min<long long>(items, sms);
+  kern<<<grid, tc::kThreads, smem, stream>>>(pt, tmk, tmv, tmq, num_seqs, q_tma ? 1 : 0);
   return cudaGetLastError();
 }
 
