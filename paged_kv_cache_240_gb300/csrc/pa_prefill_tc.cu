@@ -3,24 +3,33 @@
 // ("PyTorch LLM Serving Engine", "What is implemented": chunked prefill; "Loading":
 // online softmax while walking the block table).
 //
-// A CTA owns 256 query rows (two tiles of 128) of one sequence's chunk and one
-// kv head: row R = c*G + j is query token c, query head kvh*G + j.  The keys the
-// rows can see are walked in tiles of 64 (four 16-token blocks), each tile used
-// by both query tiles:
-//   S_t  = Q K_t^T      tcgen05.mma M=128 N=64  K=head_dim -> TMEM (two buffers)
-//   P_t  = exp2(S_t*scale - m)   one softmax thread per row, written to shared
-//                                memory as f16/bf16 in the MMA's K-major layout
-//   O   += P_t V_t      tcgen05.mma M=128 N=head_dim K=64 -> TMEM
-// Warps: 0 = TMA producer (paged K/V tiles into a ring of stages), 1 = MMA
-// issuer (the warp runs the schedule, one elected lane issues) and tensor-memory
-// owner, 2..5 and 6..9 = softmax for query
-// tiles 0 and 1, one TMEM lane (row) per thread; the two softmax warpgroups run
-// in parallel, so one tile's exponentials overlap the other tile's MMAs.  The
-// running maximum is rescaled lazily: O (in TMEM) and the normaliser are only
-// rescaled when a row's maximum grows by more than 2^8, so the exponentials stay
-// below 256.  A parity wait only tells a barrier's current phase from the one
-// before, so every barrier is waited on at every phase, in order; every wait is
-// bounded.
+// A work item is 256 query rows (two tiles of 128) of one sequence's chunk and
+// one kv head: row R = c*G + j is query token c, query head kvh*G + j.  The keys
+// the rows can see are walked in tiles of 128 (eight 16-token blocks), each tile
+// used by both query tiles:
+//   S_q = Q_q K_t^T   tcgen05.mma M=128 N=128 K=head_dim, A and B in shared memory
+//   P_q = exp2(S_q*scale - m)   one softmax thread per row; P (f16/bf16) is written
+//                     back into the first 64 columns of S_q's tensor memory
+//   O_q += P_q V_t    tcgen05.mma M=128 N=head_dim K=128, A = P from tensor memory
+// Tensor memory (512 columns): per query tile S_q (128) and O_q (128).  Keeping P
+// in tensor memory and taking 128 keys per S MMA halves the shared-memory traffic
+// per key of a 64-key tile with P in shared memory; shared-memory bandwidth, not
+// the tensor core, bounded that design.
+//
+// Warps: warpgroup 0 = warp 0 the TMA producer (Q, and K and V tiles into separate
+// rings), warp 1 the MMA warp (it runs the schedule, one elected lane issues) and
+// tensor-memory owner, warps 2-3 idle; warpgroups 1 and 2 = softmax of query tiles
+// 0 and 1, one TMEM lane (row) per thread.  Registers move from warpgroup 0 to
+// the softmax warpgroups (setmaxnreg), which hold a row's 128 scores.
+//
+// MMA order per key tile t:  P V of tile t-1 for both query tiles, then S of tile t
+// for both.  S_q of tile t overwrites the columns holding P_q of tile t-1, so it
+// waits for that P V to complete; the other query tile's MMA runs meanwhile.  The
+// running maximum is rescaled lazily: O and the normaliser only when a row's
+// maximum grows by more than 2^8, so the exponentials stay below 256.  A parity
+// wait only tells a barrier's current phase from the one before, so every
+// barrier is waited on at every phase, in order (or provably within one phase);
+// every wait is bounded.
 #include <algorithm>
 #include <cstring>
 #include <type_traits>
@@ -32,59 +41,52 @@ namespace pa_dev {
 namespace tc {
 
 constexpr int kRows = 128;      // query rows per tile (MMA M)
-constexpr int kQTiles = 2;      // query tiles per CTA
+constexpr int kQTiles = 2;      // query tiles per item
 constexpr int kCtaRows = kQTiles * kRows;
-constexpr int kKeys = 64;       // keys per tile (MMA N of S, K of P V)
-constexpr int kTileBlocks = kKeys / kBlock;
-constexpr int kNS = 3;          // K/V stages
+constexpr int kKeys = 128;      // keys per tile (MMA N of S, K of P V)
+constexpr int kTileBlocks = kKeys / kBlock;  // 8
+constexpr int kKS = 3;          // K stages
+constexpr int kVS = 2;          // V stages
+constexpr int kFlagRing = 8;    // tiles whose block-validity masks are kept
 constexpr int kSoftmaxThreads = 128;  // per query tile
-constexpr int kThreads = 64 + kQTiles * kSoftmaxThreads;  // 10 warps
+constexpr int kThreads = 128 + kQTiles * kSoftmaxThreads;  // 12 warps, 3 warpgroups
+constexpr int kLaunchRegs = 168;      // registers per thread at launch (65536 / 384)
+constexpr int kCtlRegs = 80;          // warpgroup 0 after setmaxnreg.dec
+constexpr int kSoftmaxRegs = 208;     // softmax warpgroups after setmaxnreg.inc
+static_assert(128 * kCtlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs,
+              "the register split must fit the launch's registers");
+static_assert(kCtlRegs + 2 * kSoftmaxRegs <= 512, "per sub-partition register file");
 constexpr float kLazyRescale = 8.0f;  // log2 of the growth that forces a rescale
 constexpr float kNoMax = -1.0e30f;    // running-maximum sentinel: 2^(-inf - kNoMax) = 0
 constexpr int kMaxPlan = 512;         // (sequence, tile) pairs the CTA orders by cost
-constexpr int kItemCost = 2;          // per-item overhead, in key tiles
+constexpr int kItemCost = 1;          // per-item overhead, in key tiles
 
 template <int D>
 struct Layout {
   static constexpr int kChunks = D / 64;               // 128-byte chunks of a row
   static constexpr int kQBytes = kRows * D * 2;        // per tile: [chunk][128 rows][128 B]
   static constexpr int kKVChunk = kKeys * 128;         // one chunk of a K or V tile
-  static constexpr int kKVBytes = kChunks * kKVChunk;  // [chunk][64 rows][128 B]
-  static constexpr int kStageBytes = 2 * kKVBytes;     // K then V
-  static constexpr int kPBytes = kRows * kKeys * 2;    // [128 rows][128 B]
+  static constexpr int kKVBytes = kChunks * kKVChunk;  // [chunk][128 keys][128 B]
   static constexpr int kQOff = 0;
-  static constexpr int kStageOff = kQOff + kQTiles * kQBytes;
-  static constexpr int kPOff = kStageOff + kNS * kStageBytes;  // [tile][buffer]
-  static constexpr int kBarOff = kPOff + kQTiles * 2 * kPBytes;
-  // barriers: kv_full[NS], kv_free[NS], q_full, q_free, then per query tile
-  // s_full[2], s_free[2], p_full[2], p_free[2]
-  static constexpr int kTileBars = 8;
-  static constexpr int kNumBars = 2 * kNS + 2 + kQTiles * kTileBars;
-  static constexpr int kFlagOff = kBarOff + kNumBars * 8;  // valid flags [NS][4] ints
-  static constexpr int kTmemSlotOff = kFlagOff + kNS * kTileBlocks * 4;
+  static constexpr int kKOff = kQOff + kQTiles * kQBytes;
+  static constexpr int kVOff = kKOff + kKS * kKVBytes;
+  static constexpr int kBarOff = kVOff + kVS * kKVBytes;
+  // barriers: k_full[KS], k_free[KS], v_full[VS], v_free[VS], q_full, q_free,
+  // then per query tile s_full, p_full, pv_done
+  static constexpr int kNumBars = 2 * kKS + 2 * kVS + 2 + 3 * kQTiles;
+  static constexpr int kFlagOff = kBarOff + kNumBars * 8;  // block masks [kFlagRing]
+  static constexpr int kTmemSlotOff = kFlagOff + kFlagRing * 4;
   static constexpr int kOrderOff = kTmemSlotOff + 16;  // work order [kMaxPlan] uint16
   static constexpr int kUsed = kOrderOff + kMaxPlan * 2;
   static constexpr int kBytes = kUsed + 1024;  // room to align the base to 1024
-  // tensor memory columns per query tile: S buffers 0/1, then O
-  static constexpr uint32_t kSCol0 = 0, kSCol1 = kKeys, kOCol = 2 * kKeys;
+  // tensor memory columns per query tile: S (P in its first 64), then O
+  static constexpr uint32_t kSCol = 0, kOCol = kKeys;
   static constexpr uint32_t kTileCols = 256;
   static constexpr uint32_t kTmemCols = kQTiles * kTileCols;
   static_assert(kOCol + D <= kTileCols, "tensor memory budget");
   static_assert(kBytes <= 232448, "shared memory budget");
+  static_assert(kMaxPlan * 4 <= kVS * kKVBytes, "cost scratch fits the V stages");
 };
-
-struct TileBars {
-  uint64_t *s_full, *s_free, *p_full, *p_free;
-};
-
-__device__ __forceinline__ TileBars tile_bars(uint64_t* base) {
-  TileBars b;
-  b.s_full = base;
-  b.s_free = base + 2;
-  b.p_full = base + 4;
-  b.p_free = base + 6;
-  return b;
-}
 
 // Shared-memory matrix descriptor, 128-byte swizzle (sm_100 family layout:
 // start >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride byte
@@ -113,6 +115,16 @@ __device__ __forceinline__ void mma_elect(uint32_t d_tmem, uint64_t a, uint64_t 
       "l"(a), "l"(b), "r"(id), "r"(accumulate));
 }
 
+// As mma_elect with the A operand in tensor memory: row m of A in lane m, two
+// 16-bit elements per 32-bit column (the even k in the low half).
+__device__ __forceinline__ void mma_elect_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                                 uint32_t id, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate));
+}
+
 __device__ __forceinline__ void commit_elect(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
@@ -136,21 +148,45 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
         "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      : "r"(taddr)
+      : "memory");
 #pragma unroll
   for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// 128 consecutive fp32 columns of this thread's TMEM lane, one load and one wait
+// in the same asm statement (no use of the registers can move before the wait).
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+  uint32_t r[128];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 128; i++) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
@@ -173,11 +209,45 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 64 consecutive 32-bit columns (a row of P: 128 packed 16-bit values).
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&v)[64]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]), "r"(v[32]), "r"(v[33]), "r"(v[34]), "r"(v[35]), "r"(v[36]), "r"(v[37]), "r"(v[38]), "r"(v[39]), "r"(v[40]), "r"(v[41]), "r"(v[42]), "r"(v[43]), "r"(v[44]), "r"(v[45]), "r"(v[46]), "r"(v[47]), "r"(v[48]), "r"(v[49]), "r"(v[50]), "r"(v[51]), "r"(v[52]), "r"(v[53]), "r"(v[54]), "r"(v[55]), "r"(v[56]), "r"(v[57]), "r"(v[58]), "r"(v[59]), "r"(v[60]), "r"(v[61]), "r"(v[62]), "r"(v[63])
+      : "memory");
+}
+
+// Three-input maximum and packed fp32 pairs (two IEEE operations per instruction).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // Byte offset of 16-byte unit u (0..7) of row r in a 128-byte-row swizzled chunk.
 __device__ __forceinline__ uint32_t sw_unit(int r, int u) {
   return (uint32_t)(r * 128 + (((u ^ r) & 7) << 4));
 }
-
 // One work item: 256 query rows (two tiles) of one sequence's chunk and one kv
 // head, and the key range those rows can see.
 struct Item {
@@ -266,50 +336,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::kBarOff);
-  uint64_t* kv_full = bars;
-  uint64_t* kv_free = bars + kNS;
-  uint64_t* q_full = bars + 2 * kNS;
+  uint64_t* k_full = bars;
+  uint64_t* k_free = k_full + kKS;
+  uint64_t* v_full = k_free + kKS;
+  uint64_t* v_free = v_full + kVS;
+  uint64_t* q_full = v_free + kVS;
   uint64_t* q_free = q_full + 1;
-  uint64_t* tbar0 = q_full + 2;  // per-tile barriers follow
-  int* vflags = reinterpret_cast<int*>(smem + LY::kFlagOff);
+  uint64_t* s_full = q_free + 1;          // [kQTiles]: S_q of the current tile is in TMEM
+  uint64_t* p_full = s_full + kQTiles;    // [kQTiles]: P_q is in TMEM (128 arrivals)
+  uint64_t* pv_done = p_full + kQTiles;   // [kQTiles]: the P V that read P_q finished
+  uint32_t* bmask = reinterpret_cast<uint32_t*>(smem + LY::kFlagOff);  // loaded blocks per tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::kTmemSlotOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
-  const bool reporter = threadIdx.x == 0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNS; i++) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_free[i], 1);
+    for (int i = 0; i < kKS; i++) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_free[i], 1);
+    }
+    for (int i = 0; i < kVS; i++) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_free[i], 1);
     }
     mbar_init(q_full, 32);  // the producer warp's lanes
     mbar_init(q_free, 1);
     for (int q = 0; q < kQTiles; q++) {
-      const TileBars tb = tile_bars(tbar0 + q * LY::kTileBars);
-      for (int i = 0; i < 2; i++) {
-        mbar_init(&tb.s_full[i], 1);
-        mbar_init(&tb.s_free[i], kSoftmaxThreads);
-        mbar_init(&tb.p_full[i], kSoftmaxThreads);
-        mbar_init(&tb.p_free[i], 1);
-      }
+      mbar_init(&s_full[q], 1);
+      mbar_init(&p_full[q], kSoftmaxThreads);
+      mbar_init(&pv_done[q], 1);
     }
     fence_mbar_init();
   }
-  if (warp == 1) {  // tensor memory: per query tile, S (2 x 64 columns) and O
+  if (warp == 1) {  // tensor memory: per query tile, S (P in its first half) and O
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(LY::kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  // the work order (the P buffers serve as scratch: nothing has written them yet)
+  // the work order (the V stages serve as scratch: nothing has been loaded yet)
   WorkList wl;
   wl.num_pairs = num_seqs * p.q_tiles;
   wl.kv_heads = p.num_kv_heads;
   wl.q_tiles = p.q_tiles;
   wl.order = nullptr;
   if (wl.num_pairs <= kMaxPlan) {
-    int* cost = reinterpret_cast<int*>(smem + LY::kPOff);
+    int* cost = reinterpret_cast<int*>(smem + LY::kVOff);
     uint16_t* order = reinterpret_cast<uint16_t*>(smem + LY::kOrderOff);
     for (int j = threadIdx.x; j < wl.num_pairs; j += kThreads) {
       const Item it = item_info(p, j / p.q_tiles, 0, j % p.q_tiles, false);
@@ -333,166 +406,201 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   bool timed_out = false;
 
-  if (warp == 0) {
-    // ---------------- producer: each item's Q, then its K/V tiles of four blocks
-    int g = 0, k = 0;  // tiles and items with tiles so far
-    int n, kvh, tile;
-    for (int j = 0; !timed_out && wl.at(j, n, kvh, tile); j++) {
-      const Item it = item_info(p, n, kvh, tile, reporter);
-      if (!it.valid || it.ntiles == 0) continue;
-      // Q of this item, once the previous item's S MMAs have finished with it
-      if (k > 0 && !warp_wait(q_free, (k - 1) & 1)) {
-        timed_out = true;
-        break;
-      }
-      uint8_t* qs = smem + LY::kQOff;
-      if (q_tma) {
-        // box [128/G tokens][G heads][64 columns] = 128 rows of the tile
-        if (lane == 0) mbar_arrive_expect_tx(q_full, kQTiles * LY::kQBytes);
-        __syncwarp();
-        if (lane < kQTiles * LY::kChunks) {
-          const int q = lane / LY::kChunks, h = lane % LY::kChunks;
-          tma_load_3d(qs + q * LY::kQBytes + h * (kRows * 128), &tmq, 64 * h, it.kvh * G,
-                      it.q0 + (it.R0 + q * kRows) / G, q_full);
-        }
-        if (lane != 0) mbar_arrive(q_full);
-      } else {
-        const QT* qg = static_cast<const QT*>(p.q);
-        for (int r = lane; r < kCtaRows; r += 32) {
-          const int R = it.R0 + r;
-          const bool rv = R < it.nrows;
-          const long long orow =
-              rv ? (long long)(it.q0 + R / G) * p.num_q_heads + it.kvh * G + R % G : 0;
-          const uint4* src = reinterpret_cast<const uint4*>(qg + orow * D);
-          uint8_t* qt = qs + (r / kRows) * LY::kQBytes;
-#pragma unroll
-          for (int u = 0; u < D / 8; u++)
-            cp_async_16_or_zero(qt + (u / 8) * (kRows * 128) + sw_unit(r % kRows, u % 8), src + u,
-                                rv);
-        }
-        cp_async_wait_all();
-        fence_proxy_async();
-        mbar_arrive(q_full);
-      }
-      k++;
-      // K/V tiles; block ids 32 at a time (lane l holds entry 32*b + l of batch
-      // b), the next batch loaded while this one is used
-      const int32_t* table =
-          p.block_tables + (long long)it.n * p.max_blocks_per_seq + it.first;
-      const int nblk = it.hi_u / kBlock - it.first + 1;
-      constexpr int kTilesPerBatch = 32 / kTileBlocks;
-      auto batch = [&](int b) { return 32 * b + lane < nblk ? table[32 * b + lane] : -1; };
-      int ids = batch(0), ids_next = batch(1);
-      for (int t = 0; t < it.ntiles; t++, g++) {
-        const int st = g % kNS;
-        if (t > 0 && t % kTilesPerBatch == 0) {
-          ids = ids_next;
-          ids_next = batch(t / kTilesPerBatch + 1);
-        }
-        const int from = __shfl_sync(0xffffffffu, ids, (kTileBlocks * t + lane) & 31);
-        const bool inside = lane < kTileBlocks && kTileBlocks * t + lane < nblk;
-        const int mine = inside ? from : -1;
-        const bool ok = inside && mine >= 0 && mine < p.num_blocks;
-        if (g >= kNS && !warp_wait(&kv_free[st], ((g / kNS) - 1) & 1)) {
+  if (warp < 4) {
+    setmaxnreg_dec<kCtlRegs>();
+    if (warp == 0) {
+      // ---------------- producer: each item's Q, then its K and V tiles
+      int gk = 0, gv = 0, k = 0;  // K tiles, V tiles and items with tiles so far
+      int n, kvh, tile;
+      for (int j = 0; !timed_out && wl.at(j, n, kvh, tile); j++) {
+        const Item it = item_info(p, n, kvh, tile, threadIdx.x == 0);
+        if (!it.valid || it.ntiles == 0) continue;
+        // Q of this item, once the previous item's S MMAs have finished with it
+        if (k > 0 && !warp_wait(q_free, (k - 1) & 1)) {
           timed_out = true;
           break;
         }
-        if (lane < kTileBlocks) {
-          vflags[st * kTileBlocks + lane] = ok ? 1 : 0;
-          if (inside && !ok) set_flag(p.err, PA_FLAG_BLOCK_ID);
-        }
-        __syncwarp();  // every lane's flag is written before lane 0 arms the stage
-        const unsigned okmask = __ballot_sync(0xffffffffu, ok);
-        if (lane == 0)
-          mbar_arrive_expect_tx(&kv_full[st], __popc(okmask) * 2u * LY::kKVBytes / kTileBlocks);
-        __syncwarp();
-        if (ok) {
-          uint8_t* kbase = smem + LY::kStageOff + st * LY::kStageBytes;
-          uint8_t* vbase = kbase + LY::kKVBytes;
-          const int row0 = (mine * p.num_kv_heads + it.kvh) * kBlock;
-#pragma unroll
-          for (int h = 0; h < LY::kChunks; h++) {
-            tma_load_2d(kbase + h * LY::kKVChunk + lane * kBlock * 128, &tmk, 64 * h, row0,
-                        &kv_full[st]);
-            tma_load_2d(vbase + h * LY::kKVChunk + lane * kBlock * 128, &tmv, 64 * h, row0,
-                        &kv_full[st]);
+        uint8_t* qs = smem + LY::kQOff;
+        if (q_tma) {
+          // box [128/G tokens][G heads][64 columns] = 128 rows of the tile
+          if (lane == 0) mbar_arrive_expect_tx(q_full, kQTiles * LY::kQBytes);
+          __syncwarp();
+          if (lane < kQTiles * LY::kChunks) {
+            const int q = lane / LY::kChunks, h = lane % LY::kChunks;
+            tma_load_3d(qs + q * LY::kQBytes + h * (kRows * 128), &tmq, 64 * h, it.kvh * G,
+                        it.q0 + (it.R0 + q * kRows) / G, q_full);
           }
-        }
-      }
-    }
-    // no copy may still be landing in shared memory when the CTA exits; the last
-    // kNS tiles issued and the last Q are their barriers' current phases
-    if (lane == 0) {
-      for (int t = g > kNS ? g - kNS : 0; t < g; t++)
-        if (!mbar_wait(&kv_full[t % kNS], (t / kNS) & 1)) break;
-      if (k > 0) mbar_wait(q_full, (k - 1) & 1);
-    }
-    if (timed_out && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
-  } else if (warp == 1) {
-    // ---------------- MMA issuer (the whole warp; one elected lane issues)
-    const uint32_t idS = idesc<BF>(kRows, kKeys, false);
-    const uint32_t idO = idesc<BF>(kRows, D, true);
-    // O_q (+)= P_{q,g} V_g; `first` starts a new accumulation
-    auto pv = [&](int q, int g, bool first) -> bool {
-      const TileBars tb = tile_bars(tbar0 + q * LY::kTileBars);
-      if (!warp_wait(&tb.p_full[g & 1], (g >> 1) & 1)) return false;
-      fence_after();
-      const uint32_t sP = smem_u32(smem + LY::kPOff + (2 * q + (g & 1)) * LY::kPBytes);
-      const uint32_t sV =
-          smem_u32(smem + LY::kStageOff + (g % kNS) * LY::kStageBytes) + LY::kKVBytes;
-      const uint32_t dO = tmem + q * LY::kTileCols + LY::kOCol;
+          if (lane != 0) mbar_arrive(q_full);
+        } else {
+          const QT* qg = static_cast<const QT*>(p.q);
+          for (int r = lane; r < kCtaRows; r += 32) {
+            const int R = it.R0 + r;
+            const bool rv = R < it.nrows;
+            const long long orow =
+                rv ? (long long)(it.q0 + R / G) * p.num_q_heads + it.kvh * G + R % G : 0;
+            const uint4* src = reinterpret_cast<const uint4*>(qg + orow * D);
+            uint8_t* qt = qs + (r / kRows) * LY::kQBytes;
 #pragma unroll
-      for (int s = 0; s < kKeys / 16; s++)
-        mma_elect(dO, sw128_desc(sP + 32 * s, 16, 1024),
-                  sw128_desc(sV + 2048 * s, LY::kKVChunk, 1024), idO,
-                  (!first || s > 0) ? 1u : 0u);
-      commit_elect(&tb.p_free[g & 1]);
-      return true;
-    };
-    bool ok = true;
-    int g = 0, k = 0;
-    int n, kvh, tile;
-    for (int j = 0; ok && wl.at(j, n, kvh, tile); j++) {
-      const Item it = item_info(p, n, kvh, tile, false);
-      if (!it.valid || it.ntiles == 0) continue;
-      ok = warp_wait(q_full, k & 1);
-      k++;
-      for (int t = 0; t < it.ntiles && ok; t++, g++) {
-        const int st = g % kNS;
-        ok = warp_wait(&kv_full[st], (g / kNS) & 1);
-        const uint32_t sK = smem_u32(smem + LY::kStageOff + st * LY::kStageBytes);
-        for (int q = 0; q < kQTiles && ok; q++) {
-          const TileBars tb = tile_bars(tbar0 + q * LY::kTileBars);
-          if (g >= 2) ok = warp_wait(&tb.s_free[g & 1], ((g - 2) >> 1) & 1);
-          if (!ok) break;
-          fence_after();
-          const uint32_t sQ = smem_u32(smem + LY::kQOff + q * LY::kQBytes);
-          const uint32_t dS = tmem + q * LY::kTileCols + ((g & 1) ? LY::kSCol1 : LY::kSCol0);
+            for (int u = 0; u < D / 8; u++)
+              cp_async_16_or_zero(qt + (u / 8) * (kRows * 128) + sw_unit(r % kRows, u % 8),
+                                  src + u, rv);
+          }
+          cp_async_wait_all();
+          fence_proxy_async();
+          mbar_arrive(q_full);
+        }
+        k++;
+        // block ids 32 at a time (lane l holds entry 32*b + l of batch b), the
+        // next batch loaded while this one is used
+        const int32_t* table =
+            p.block_tables + (long long)it.n * p.max_blocks_per_seq + it.first;
+        const int nblk = it.hi_u / kBlock - it.first + 1;
+        constexpr int kTilesPerBatch = 32 / kTileBlocks;
+        auto batch = [&](int b) { return 32 * b + lane < nblk ? table[32 * b + lane] : -1; };
+        int ids = batch(0), ids_next = batch(1);
+        for (int t = 0; t < it.ntiles; t++) {
+          if (t > 0 && t % kTilesPerBatch == 0) {
+            ids = ids_next;
+            ids_next = batch(t / kTilesPerBatch + 1);
+          }
+          const int from = __shfl_sync(0xffffffffu, ids, (kTileBlocks * t + lane) & 31);
+          const bool inside = lane < kTileBlocks && kTileBlocks * t + lane < nblk;
+          const int mine = inside ? from : -1;
+          const bool ok = inside && mine >= 0 && mine < p.num_blocks;
+          if (inside && !ok) set_flag(p.err, PA_FLAG_BLOCK_ID);
+          const unsigned okmask = __ballot_sync(0xffffffffu, ok);
+          const uint32_t tile_bytes = __popc(okmask) * LY::kChunks * kBlock * 128;
+          const int row0 = (mine * p.num_kv_heads + it.kvh) * kBlock;
+          // K of tile gk
+          const int ks = gk % kKS;
+          if (gk >= kKS && !warp_wait(&k_free[ks], ((gk / kKS) - 1) & 1)) {
+            timed_out = true;
+            break;
+          }
+          if (lane == 0) {
+            bmask[gk % kFlagRing] = okmask;
+            mbar_arrive_expect_tx(&k_full[ks], tile_bytes);
+          }
+          __syncwarp();
+          if (ok) {
+            uint8_t* kbase = smem + LY::kKOff + ks * LY::kKVBytes;
 #pragma unroll
-          for (int s = 0; s < D / 16; s++)
-            mma_elect(dS, sw128_desc(sQ + (s / 4) * (kRows * 128) + (s % 4) * 32, 16, 1024),
-                      sw128_desc(sK + (s / 4) * LY::kKVChunk + (s % 4) * 32, 16, 1024), idS,
-                      s > 0 ? 1u : 0u);
-          commit_elect(&tb.s_full[g & 1]);
-        }
-        if (ok && t == it.ntiles - 1) commit_elect(q_free);  // Q is no longer read
-        if (ok && t >= 1) {
-          for (int q = 0; q < kQTiles && ok; q++) ok = pv(q, g - 1, t == 1);
-          if (ok) commit_elect(&kv_free[(g - 1) % kNS]);
+            for (int h = 0; h < LY::kChunks; h++)
+              tma_load_2d(kbase + h * LY::kKVChunk + lane * kBlock * 128, &tmk, 64 * h, row0,
+                          &k_full[ks]);
+          }
+          gk++;
+          // V of tile gv (= gk - 1)
+          const int vs = gv % kVS;
+          if (gv >= kVS && !warp_wait(&v_free[vs], ((gv / kVS) - 1) & 1)) {
+            timed_out = true;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(&v_full[vs], tile_bytes);
+          __syncwarp();
+          if (ok) {
+            uint8_t* vbase = smem + LY::kVOff + vs * LY::kKVBytes;
+#pragma unroll
+            for (int h = 0; h < LY::kChunks; h++)
+              tma_load_2d(vbase + h * LY::kKVChunk + lane * kBlock * 128, &tmv, 64 * h, row0,
+                          &v_full[vs]);
+          }
+          gv++;
         }
       }
-      if (ok) {
-        for (int q = 0; q < kQTiles && ok; q++) ok = pv(q, g - 1, it.ntiles == 1);
-        if (ok) commit_elect(&kv_free[(g - 1) % kNS]);
+      // no copy may still be landing in shared memory when the CTA exits; the
+      // last fills issued are their barriers' current phases
+      if (lane == 0) {
+        for (int t = gk > kKS ? gk - kKS : 0; t < gk; t++)
+          if (!mbar_wait(&k_full[t % kKS], (t / kKS) & 1)) break;
+        for (int t = gv > kVS ? gv - kVS : 0; t < gv; t++)
+          if (!mbar_wait(&v_full[t % kVS], (t / kVS) & 1)) break;
+        if (k > 0) mbar_wait(q_full, (k - 1) & 1);
       }
+      if (timed_out && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
+    } else if (warp == 1) {
+      // ---------------- MMA warp (one elected lane issues)
+      const uint32_t idS = idesc<BF>(kRows, kKeys, false);
+      const uint32_t idO = idesc<BF>(kRows, D, true);
+      // descriptors advance by adding (byte offset >> 4) to the start-address
+      // field: every shared-memory address here is below 256 KB, so no carry
+      const uint64_t dQ0 = sw128_desc(smem_u32(smem + LY::kQOff), 16, 1024);
+      const uint64_t dK0 = sw128_desc(smem_u32(smem + LY::kKOff), 16, 1024);
+      const uint64_t dV0 = sw128_desc(smem_u32(smem + LY::kVOff), LY::kKVChunk, 1024);
+      bool started0 = false, started1 = false;  // O_q holds this item's first product
+      // O_q (+)= P_q V of tile gg, skipping the blocks that were not loaded
+      auto pv = [&](int q, int gg, bool& started) -> bool {
+        if (!warp_wait(&p_full[q], gg & 1)) return false;
+        fence_after();
+        const uint64_t dV = dV0 + (uint64_t)(((gg % kVS) * LY::kKVBytes) >> 4);
+        const uint32_t mask = bmask[gg % kFlagRing];
+        const uint32_t dO = tmem + q * LY::kTileCols + LY::kOCol;
+        const uint32_t aP = tmem + q * LY::kTileCols + LY::kSCol;
+        if (mask == 0xFFu && started) {
+#pragma unroll
+          for (int s = 0; s < kTileBlocks; s++)
+            mma_elect_tmem_a(dO, aP + 8 * s, dV + (uint64_t)((2048 * s) >> 4), idO, 1u);
+        } else {
+#pragma unroll
+          for (int s = 0; s < kTileBlocks; s++)
+            if ((mask >> s) & 1u) {
+              mma_elect_tmem_a(dO, aP + 8 * s, dV + (uint64_t)((2048 * s) >> 4), idO,
+                               started ? 1u : 0u);
+              started = true;
+            }
+        }
+        commit_elect(&pv_done[q]);
+        return true;
+      };
+      auto pv_both = [&](int gg) -> bool {
+        bool r = warp_wait(&v_full[gg % kVS], (gg / kVS) & 1);
+        if (r) r = pv(0, gg, started0);
+        if (r) r = pv(1, gg, started1);
+        if (r) commit_elect(&v_free[gg % kVS]);
+        return r;
+      };
+      static_assert(kQTiles == 2, "the MMA schedule is written for two query tiles");
+      bool ok = true;
+      int g = 0, k = 0;
+      int n, kvh, tile;
+      for (int j = 0; ok && wl.at(j, n, kvh, tile); j++) {
+        const Item it = item_info(p, n, kvh, tile, false);
+        if (!it.valid || it.ntiles == 0) continue;
+        ok = warp_wait(q_full, k & 1);
+        k++;
+        started0 = started1 = false;
+        for (int t = 0; t < it.ntiles && ok; t++, g++) {
+          if (t >= 1) ok = pv_both(g - 1);  // P V of the previous tile
+          if (ok) ok = warp_wait(&k_full[g % kKS], (g / kKS) & 1);
+          const uint64_t dK = dK0 + (uint64_t)(((g % kKS) * LY::kKVBytes) >> 4);
+#pragma unroll
+          for (int q = 0; q < kQTiles; q++) {
+            // S_q overwrites the columns that held P_q of tile g-1
+            if (ok && g >= 1) ok = warp_wait(&pv_done[q], (g - 1) & 1);
+            if (!ok) break;
+            fence_after();
+            const uint64_t dQ = dQ0 + (uint64_t)((q * LY::kQBytes) >> 4);
+            const uint32_t dS = tmem + q * LY::kTileCols + LY::kSCol;
+#pragma unroll
+            for (int s = 0; s < D / 16; s++)
+              mma_elect(dS, dQ + (uint64_t)(((s / 4) * (kRows * 128) + (s % 4) * 32) >> 4),
+                        dK + (uint64_t)(((s / 4) * LY::kKVChunk + (s % 4) * 32) >> 4), idS,
+                        s > 0 ? 1u : 0u);
+            commit_elect(&s_full[q]);
+          }
+          if (ok) commit_elect(&k_free[g % kKS]);
+          if (ok && t == it.ntiles - 1) commit_elect(q_free);  // Q is no longer read
+        }
+        if (ok) ok = pv_both(g - 1);  // the item's last tile
+      }
+      if (!ok && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
+      __syncwarp();
     }
-    if (!ok && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
-    __syncwarp();
   } else {
+    setmaxnreg_inc<kSoftmaxRegs>();
     // ---------------- softmax: query tile q, thread <-> row (TMEM lane 32*(warp%4) + lane)
-    const int q = (warp - 2) / 4;
-    const TileBars tb = tile_bars(tbar0 + q * LY::kTileBars);
-    const int stid = threadIdx.x - 64 - q * kSoftmaxThreads;  // 0..127 within the tile
+    const int q = (warp - 4) / 4;
+    const int stid = threadIdx.x - 128 - q * kSoftmaxThreads;  // 0..127 within the tile
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_base = tmem + q * LY::kTileCols + ((uint32_t)(32 * (warp & 3)) << 16);
     const float sc = p.scale_log2;
@@ -517,77 +625,58 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u = 0; u < D / 8; u++) reinterpret_cast<uint4*>(dst)[u] = make_uint4(0, 0, 0, 0);
         continue;
       }
-      // p_free[b] completes when the P V that read P buffer b has finished, and
-      // with it every earlier MMA.  Tile g waits on it for the P V of tile g-1
-      // (buffer (g-1)&1) before rescaling O, and for the P V of tile g-2 (buffer
-      // g&1) before writing P.  Per buffer these are successive phases, and a
-      // repeated wait on the same phase is safe: the next one needs this tile's P.
+      // the block holding position L-1 may carry unwritten slots past it
+      const int tail_blk = (it.L - 1) / kBlock;
+      const int tail_rows = it.L % kBlock;  // valid rows of that block (0: all 16)
       float m_used = kNoMax, l = 0.0f;
       for (int t = 0; t < it.ntiles; t++, g++) {
-        if (!mbar_wait(&tb.s_full[g & 1], (g >> 1) & 1)) {
+        if (!mbar_wait(&s_full[q], g & 1)) {
           timed_out = true;
           break;
         }
+        // S of tile g is complete, and with it (it was issued after waiting for
+        // it) the P V of tile g-1: O holds every earlier tile
         fence_after();
-        const int pos0 = (it.first + kTileBlocks * t) * kBlock;
-        const int* vf = vflags + (g % kNS) * kTileBlocks;
-        const bool blocks_ok = vf[0] && vf[1] && vf[2] && vf[3];
+        const int blk0 = it.first + kTileBlocks * t;
+        const int pos0 = blk0 * kBlock;
+        const uint32_t mask = bmask[g % kFlagRing];
         float x[kKeys];
-        {
-          float v[32];
-          const uint32_t scol = (g & 1) ? LY::kSCol1 : LY::kSCol0;
-          tmem_ld32(lane_base + scol, v);
-#pragma unroll
-          for (int j = 0; j < 32; j++) x[j] = v[j];
-          tmem_ld32(lane_base + scol + 32, v);
-#pragma unroll
-          for (int j = 0; j < 32; j++) x[32 + j] = v[j];
-        }
-        fence_before();
-        mbar_arrive(&tb.s_free[g & 1]);  // the MMA may overwrite this S buffer now
+        tmem_ld128(lane_base + LY::kSCol, x);
         // maximum of the scaled scores this row can see; an inner tile (every key
         // visible to every row of the warp) skips the masks.  Eight partial maxima
-        // and sums keep the dependency chains short.
-        float part[8];
-        const bool inner = __all_sync(0xffffffffu, blocks_ok && pos0 >= row_lo &&
+        // (three-input max) keep the dependency chains short.
+        const bool inner = __all_sync(0xffffffffu, (mask & 0xFFu) == 0xFFu && pos0 >= row_lo &&
                                                        pos0 + kKeys - 1 <= row_hi) &&
                            sc > 0.0f;
-        if (inner) {
+        if (!inner) {
 #pragma unroll
-          for (int j = 0; j < 8; j++) part[j] = x[j];
-#pragma unroll
-          for (int j = 8; j < kKeys; j++) part[j & 7] = fmaxf(part[j & 7], x[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; j++) part[j] = -INFINITY;
-#pragma unroll
-          for (int j = 0; j < kKeys; j++) {
-            const int kp = pos0 + j;
-            const bool vis = kp >= row_lo && kp <= row_hi && vf[j / kBlock];
-            x[j] = vis ? x[j] * sc : -INFINITY;
-            part[j & 7] = fmaxf(part[j & 7], x[j]);
+          for (int i = 0; i < kKeys; i++) {
+            const int kp = pos0 + i;
+            const bool vis = kp >= row_lo && kp <= row_hi && ((mask >> (i / kBlock)) & 1u);
+            x[i] = vis ? x[i] * sc : -INFINITY;
           }
         }
-        float mt = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
-                         fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
+        float pm[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) pm[j] = fmaxf(x[j], x[j + 8]);
+#pragma unroll
+        for (int k16 = 1; k16 < kKeys / 16; k16++)
+#pragma unroll
+          for (int j = 0; j < 8; j++) pm[j] = fmax3(pm[j], x[16 * k16 + j], x[16 * k16 + 8 + j]);
+        float mt = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
         if (inner) mt *= sc;
         // lazy rescale: only when this row's maximum grew by more than 2^8
         const bool need = mt > m_used + kLazyRescale;
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = need ? mt : m_used;
           const float factor = need ? fast_exp2(m_used - m_new) : 1.0f;
-          if (t > 0) {  // O holds this item's tiles < t: wait for the last P V, scale O
-            if (!mbar_wait(&tb.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1)) {
-              timed_out = true;
-              break;
-            }
-            fence_after();
+          if (t > 0) {  // O holds this item's tiles < t: scale it in place
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
               float v[32];
               tmem_ld32(lane_base + LY::kOCol + c0, v);
 #pragma unroll
-              for (int j = 0; j < 32; j++) v[j] *= factor;
+              for (int i = 0; i < 32; i++) v[i] *= factor;
               tmem_st32(lane_base + LY::kOCol + c0, v);
             }
           }
@@ -595,57 +684,52 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_used = m_new;
         }
         // inner tiles hold raw scores (the scale is folded into one FFMA), edge
-        // tiles already-scaled ones (-inf where masked)
-        const float mul = inner ? sc : 1.0f;
-        const float sub = -m_used;
+        // tiles already-scaled ones (-inf where masked); pairs of keys share one
+        // packed FMA and one packed add into four pairs of partial sums
+        const unsigned long long mul2 = f2pack(inner ? sc : 1.0f, inner ? sc : 1.0f);
+        const unsigned long long sub2 = f2pack(-m_used, -m_used);
+        unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pk[kKeys / 2];
 #pragma unroll
-        for (int j = 0; j < 8; j++) part[j] = 0.0f;
+        for (int i = 0; i < kKeys; i += 2) {
+          float a0, a1;
+          f2unpack(ffma2(f2pack(x[i], x[i + 1]), mul2, sub2), a0, a1);
+          const float e0 = fast_exp2(a0), e1 = fast_exp2(a1);
+          acc[(i / 2) & 3] = fadd2(acc[(i / 2) & 3], f2pack(e0, e1));
+          pk[i / 2] = pack2<BF>(e0, e1);
+        }
+        {
+          float sp[8];
 #pragma unroll
-        for (int j = 0; j < kKeys; j++) {
-          x[j] = fast_exp2(fmaf(x[j], mul, sub));
-          part[j & 7] += x[j];
+          for (int j = 0; j < 4; j++) f2unpack(acc[j], sp[2 * j], sp[2 * j + 1]);
+          l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
         }
-        l += ((part[0] + part[1]) + (part[2] + part[3])) +
-             ((part[4] + part[5]) + (part[6] + part[7]));
-        // P buffer g&1 was last read by the P V of tile g-2
-        if (g >= 2 && !mbar_wait(&tb.p_free[g & 1], ((g - 2) >> 1) & 1)) {
-          timed_out = true;
-          break;
-        }
-        // P row -> shared memory (f16/bf16, K-major swizzled)
-        uint8_t* prow = smem + LY::kPOff + (2 * q + (g & 1)) * LY::kPBytes;
-#pragma unroll
-        for (int u = 0; u < kKeys / 8; u++) {
-          uint4 pk;
-          pk.x = pack2<BF>(x[8 * u + 0], x[8 * u + 1]);
-          pk.y = pack2<BF>(x[8 * u + 2], x[8 * u + 3]);
-          pk.z = pack2<BF>(x[8 * u + 4], x[8 * u + 5]);
-          pk.w = pack2<BF>(x[8 * u + 6], x[8 * u + 7]);
-          *reinterpret_cast<uint4*>(prow + sw_unit(row, u)) = pk;
-        }
-        // V rows of keys no row can see (before the window, past the context,
-        // blocks not in the pool) may hold garbage: zero them so 0 * V stays 0.
-        // Both query tiles read the stage; tile 0's warps clear it, and the MMA
-        // warp waits for tile 0's P before either tile's P V.
-        const bool edge = pos0 < it.lo_u || pos0 + kKeys - 1 > it.hi_u || !blocks_ok;
-        if (edge && q == 0) {
-          uint8_t* vbase = smem + LY::kStageOff + (g % kNS) * LY::kStageBytes + LY::kKVBytes;
-          for (int idx = stid; idx < kKeys * LY::kChunks * 8; idx += kSoftmaxThreads) {
-            const int key = idx / (LY::kChunks * 8);
-            const int rest = idx % (LY::kChunks * 8);
-            const int kp = pos0 + key;
-            if (kp < it.lo_u || kp > it.hi_u || !vf[key / kBlock])
-              *reinterpret_cast<uint4*>(vbase + (rest / 8) * LY::kKVChunk +
-                                        sw_unit(key, rest % 8)) = make_uint4(0, 0, 0, 0);
+        // P over the first 64 columns of S (this thread's S values are all read)
+        tmem_st64(lane_base + LY::kSCol, pk);
+        // unwritten slots past L-1 in a loaded block: zero their V rows, so that
+        // 0 * V stays 0 (query tile 0's warps; the MMA warp waits for both tiles' P)
+        if (q == 0 && tail_rows != 0 && tail_blk >= blk0 && tail_blk < blk0 + kTileBlocks &&
+            ((mask >> (tail_blk - blk0)) & 1u)) {
+          if (!mbar_wait(&v_full[g % kVS], (g / kVS) & 1)) {
+            timed_out = true;
+            break;
           }
+          uint8_t* vbase = smem + LY::kVOff + (g % kVS) * LY::kKVBytes;
+          const int nz = (kBlock - tail_rows) * LY::kChunks * 8;
+          for (int idx = stid; idx < nz; idx += kSoftmaxThreads) {
+            const int key = (tail_blk - blk0) * kBlock + tail_rows + idx / (LY::kChunks * 8);
+            const int rest = idx % (LY::kChunks * 8);
+            *reinterpret_cast<uint4*>(vbase + (rest / 8) * LY::kKVChunk + sw_unit(key, rest % 8)) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
         }
-        fence_proxy_async();
         fence_before();
-        mbar_arrive(&tb.p_full[g & 1]);
+        mbar_arrive(&p_full[q]);
       }
       if (timed_out) break;
       // epilogue: wait for this item's last P V (tile g-1)
-      if (!mbar_wait(&tb.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1)) {
+      if (!mbar_wait(&pv_done[q], (g - 1) & 1)) {
         timed_out = true;
         break;
       }
@@ -658,12 +742,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rvalid) {
 #pragma unroll
           for (int u = 0; u < 4; u++) {
-            uint4 pk;
-            pk.x = pack2<BF>(v[8 * u + 0] * inv, v[8 * u + 1] * inv);
-            pk.y = pack2<BF>(v[8 * u + 2] * inv, v[8 * u + 3] * inv);
-            pk.z = pack2<BF>(v[8 * u + 4] * inv, v[8 * u + 5] * inv);
-            pk.w = pack2<BF>(v[8 * u + 6] * inv, v[8 * u + 7] * inv);
-            *reinterpret_cast<uint4*>(dst + c0 + 8 * u) = pk;
+            float w[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) w[i] = l > 0.0f ? v[8 * u + i] * inv : 0.0f;
+            uint4 o4;
+            o4.x = pack2<BF>(w[0], w[1]);
+            o4.y = pack2<BF>(w[2], w[3]);
+            o4.z = pack2<BF>(w[4], w[5]);
+            o4.w = pack2<BF>(w[6], w[7]);
+            *reinterpret_cast<uint4*>(dst + c0 + 8 * u) = o4;
           }
         }
       }
@@ -720,6 +807,15 @@ cudaError_t launch_prefill_tc(const AttnParams& p, const CUtensorMap& tmk,
   auto kern = tc::pa_prefill_tc_kernel<D, QT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  // setmaxnreg moves registers between warpgroups inside the CTA's launch
+  // allocation; an increase beyond it would wait forever, so the compiled
+  // register count must cover the split before anything is launched
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if ((long long)fa.numRegs * tc::kThreads <
+      128LL * tc::kCtlRegs + (long long)tc::kQTiles * tc::kSoftmaxThreads * tc::kSoftmaxRegs)
+    return cudaErrorInvalidConfiguration;
   AttnParams pt = p;
   pt.q_tiles = (int)(((long long)p.max_q_len * p.group + tc::kCtaRows - 1) / tc::kCtaRows);
   const long long items = (long long)pt.q_tiles * pt.num_kv_heads * num_seqs;
