@@ -22,9 +22,10 @@
 // 0 and 1, one TMEM lane (row) per thread.  Registers move from warpgroup 0 to
 // the softmax warpgroups (setmaxnreg), which hold a row's 128 scores.
 //
-// MMA order per key tile t:  P V of tile t-1 for both query tiles, then S of tile t
-// for both.  S_q of tile t overwrites the columns holding P_q of tile t-1, so it
-// waits for that P V to complete; the other query tile's MMA runs meanwhile.  The
+// MMA order per key tile t:  P V_0 of tile t-1, S_0 of t, P V_1 of t-1, S_1 of t
+// (P V_1 moves ahead of S_0 when its P is ready).  S_q of tile t overwrites the
+// columns holding P_q of tile t-1, so it waits for that P V to complete; queued
+// MMAs of the other query tile run meanwhile.  The
 // running maximum is rescaled lazily: O and the normaliser only when a row's
 // maximum grows by more than 2^8, so the exponentials stay below 256.  A parity
 // wait only tells a barrier's current phase from the one before, so every
@@ -51,8 +52,8 @@ constexpr int kFlagRing = 8;    // tiles whose block-validity masks are kept
 constexpr int kSoftmaxThreads = 128;  // per query tile
 constexpr int kThreads = 128 + kQTiles * kSoftmaxThreads;  // 12 warps, 3 warpgroups
 constexpr int kLaunchRegs = 168;      // registers per thread at launch (65536 / 384)
-constexpr int kCtlRegs = 80;          // warpgroup 0 after setmaxnreg.dec
-constexpr int kSoftmaxRegs = 208;     // softmax warpgroups after setmaxnreg.inc
+constexpr int kCtlRegs = 112;          // warpgroup 0 after setmaxnreg.dec
+constexpr int kSoftmaxRegs = 192;     // softmax warpgroups after setmaxnreg.inc
 static_assert(128 * kCtlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs,
               "the register split must fit the launch's registers");
 static_assert(kCtlRegs + 2 * kSoftmaxRegs <= 512, "per sub-partition register file");
@@ -131,6 +132,19 @@ __device__ __forceinline__ void commit_elect(uint64_t* bar) {
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
           smem_u32(bar))
       : "memory");
+}
+
+// Whether the phase with the given parity has completed, without waiting
+// (every lane asks; the verdict is the warp's).
+__device__ __forceinline__ bool warp_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return __all_sync(0xffffffffu, done != 0);
 }
 
 // Bounded wait by every lane of a warp; the verdict is the warp's (uniform).
@@ -552,12 +566,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         commit_elect(&pv_done[q]);
         return true;
       };
-      auto pv_both = [&](int gg) -> bool {
-        bool r = warp_wait(&v_full[gg % kVS], (gg / kVS) & 1);
-        if (r) r = pv(0, gg, started0);
-        if (r) r = pv(1, gg, started1);
-        if (r) commit_elect(&v_free[gg % kVS]);
-        return r;
+      // S_q of tile gg; it overwrites the columns that held P_q of tile gg-1
+      auto s_mma = [&](int q, int gg, uint64_t dK) -> bool {
+        if (gg >= 1 && !warp_wait(&pv_done[q], (gg - 1) & 1)) return false;
+        fence_after();
+        const uint64_t dQ = dQ0 + (uint64_t)((q * LY::kQBytes) >> 4);
+        const uint32_t dS = tmem + q * LY::kTileCols + LY::kSCol;
+#pragma unroll
+        for (int s = 0; s < D / 16; s++)
+          mma_elect(dS, dQ + (uint64_t)(((s / 4) * (kRows * 128) + (s % 4) * 32) >> 4),
+                    dK + (uint64_t)(((s / 4) * LY::kKVChunk + (s % 4) * 32) >> 4), idS,
+                    s > 0 ? 1u : 0u);
+        commit_elect(&s_full[q]);
+        return true;
       };
       static_assert(kQTiles == 2, "the MMA schedule is written for two query tiles");
       bool ok = true;
@@ -569,29 +590,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = warp_wait(q_full, k & 1);
         k++;
         started0 = started1 = false;
+        // Per tile g: P V of tile g-1 and S of tile g for each query tile, in the
+        // order P V_0, S_0, P V_1, S_1, except that P V_1 goes first when its P is
+        // already there, so the tensor pipe always has queued work while the MMA
+        // warp waits for a P V to finish before the S that overwrites its P.
         for (int t = 0; t < it.ntiles && ok; t++, g++) {
-          if (t >= 1) ok = pv_both(g - 1);  // P V of the previous tile
-          if (ok) ok = warp_wait(&k_full[g % kKS], (g / kKS) & 1);
+          ok = warp_wait(&k_full[g % kKS], (g / kKS) & 1);
           const uint64_t dK = dK0 + (uint64_t)(((g % kKS) * LY::kKVBytes) >> 4);
-#pragma unroll
-          for (int q = 0; q < kQTiles; q++) {
-            // S_q overwrites the columns that held P_q of tile g-1
-            if (ok && g >= 1) ok = warp_wait(&pv_done[q], (g - 1) & 1);
-            if (!ok) break;
-            fence_after();
-            const uint64_t dQ = dQ0 + (uint64_t)((q * LY::kQBytes) >> 4);
-            const uint32_t dS = tmem + q * LY::kTileCols + LY::kSCol;
-#pragma unroll
-            for (int s = 0; s < D / 16; s++)
-              mma_elect(dS, dQ + (uint64_t)(((s / 4) * (kRows * 128) + (s % 4) * 32) >> 4),
-                        dK + (uint64_t)(((s / 4) * LY::kKVChunk + (s % 4) * 32) >> 4), idS,
-                        s > 0 ? 1u : 0u);
-            commit_elect(&s_full[q]);
+          if (ok && t >= 1) {
+            ok = warp_wait(&v_full[(g - 1) % kVS], ((g - 1) / kVS) & 1);
+            if (ok) ok = pv(0, g - 1, started0);
+            bool pv1 = false;
+            if (ok && warp_test(&p_full[1], (g - 1) & 1)) {
+              ok = pv(1, g - 1, started1);
+              pv1 = true;
+            }
+            if (ok) ok = s_mma(0, g, dK);
+            if (ok && !pv1) ok = pv(1, g - 1, started1);
+            if (ok) commit_elect(&v_free[(g - 1) % kVS]);
+            if (ok) ok = s_mma(1, g, dK);
+          } else if (ok) {
+            ok = s_mma(0, g, dK);
+            if (ok) ok = s_mma(1, g, dK);
           }
           if (ok) commit_elect(&k_free[g % kKS]);
           if (ok && t == it.ntiles - 1) commit_elect(q_free);  // Q is no longer read
         }
-        if (ok) ok = pv_both(g - 1);  // the item's last tile
+        if (ok) {  // the item's last tile
+          ok = warp_wait(&v_full[(g - 1) % kVS], ((g - 1) / kVS) & 1);
+          if (ok) ok = pv(0, g - 1, started0);
+          if (ok) ok = pv(1, g - 1, started1);
+          if (ok) commit_elect(&v_free[(g - 1) % kVS]);
+        }
       }
       if (!ok && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
       __syncwarp();
@@ -665,21 +695,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 8; j++) pm[j] = fmax3(pm[j], x[16 * k16 + j], x[16 * k16 + 8 + j]);
         float mt = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
         if (inner) mt *= sc;
-        // lazy rescale: only when this row's maximum grew by more than 2^8
+        // lazy rescale: only when this row's maximum grew by more than 2^8 (O is
+        // scaled below, once the scores are no longer held in registers)
         const bool need = mt > m_used + kLazyRescale;
-        if (__any_sync(0xffffffffu, need)) {
+        const bool rescale = __any_sync(0xffffffffu, need);
+        float factor = 1.0f;
+        if (rescale) {
           const float m_new = need ? mt : m_used;
-          const float factor = need ? fast_exp2(m_used - m_new) : 1.0f;
-          if (t > 0) {  // O holds this item's tiles < t: scale it in place
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              float v[32];
-              tmem_ld32(lane_base + LY::kOCol + c0, v);
-#pragma unroll
-              for (int i = 0; i < 32; i++) v[i] *= factor;
-              tmem_st32(lane_base + LY::kOCol + c0, v);
-            }
-          }
+          factor = need ? fast_exp2(m_used - m_new) : 1.0f;
           l *= factor;
           m_used = m_new;
         }
@@ -706,6 +729,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // P over the first 64 columns of S (this thread's S values are all read)
         tmem_st64(lane_base + LY::kSCol, pk);
+        if (rescale && t > 0) {
+          // O holds this item's tiles < t (their P V is complete): scale it in place
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float v[32];
+            tmem_ld32(lane_base + LY::kOCol + c0, v);
+#pragma unroll
+            for (int i = 0; i < 32; i++) v[i] *= factor;
+            tmem_st32(lane_base + LY::kOCol + c0, v);
+          }
+        }
         // unwritten slots past L-1 in a loaded block: zero their V rows, so that
         // 0 * V stays 0 (query tile 0's warps; the MMA warp waits for both tiles' P)
         if (q == 0 && tail_rows != 0 && tail_blk >= blk0 && tail_blk < blk0 + kTileBlocks &&
