@@ -36,7 +36,8 @@ sys.path.insert(0, ROOT)
 METRIC = "paged-attn decode KV-read GB/s (% of GB300 HBM peak); decode steps/sec"
 DEFAULT_WORKLOAD = "mha-7b"
 L2_BYTES = 129 * 2 ** 20
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+TRAFFIC_FILES = {"decode": os.path.join(ROOT, "profiles", "decode_traffic.json"),
+                 "prefill": os.path.join(ROOT, "profiles", "prefill_traffic.json")}
 
 
 def kernel_source_hash(files) -> str:
@@ -48,11 +49,11 @@ def kernel_source_hash(files) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
-    """DRAM bytes per pa_decode call from the committed ncu record, or None when
-    the decode sources changed since it was taken."""
+def recorded_traffic(workload, call="decode"):
+    """DRAM bytes per pa_decode (or pa_prefill_chunk) call from the committed ncu
+    record, or None when the kernel sources changed since it was taken."""
     try:
-        with open(TRAFFIC_FILE) as f:
+        with open(TRAFFIC_FILES[call]) as f:
             tr = json.load(f)
     except (OSError, ValueError):
         return None
@@ -161,7 +162,7 @@ class DeviceStep:
         nbytes = pa.pa_decode_workspace_bytes(nd, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                               w.max_blocks_per_seq, w.window)
         self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
-        self.reduce_launched = nbytes > 0
+        self.reduce_launched = nbytes > 0 and nd > 0
         torch.cuda.synchronize()
         if int(self.err[0]) != 0:
             raise RuntimeError("device flags %d while filling the cache" % int(self.err[0]))
@@ -172,13 +173,15 @@ class DeviceStep:
     OUTPUTS = ("out_dec", "out_pre")
 
     def launches_per_step(self):
-        n = 2 + (1 if self.reduce_launched else 0)
+        n = 1 + (1 if self.nd else 0) + (1 if self.reduce_launched else 0)
         return n + (1 if self.max_q else 0)
 
     def write(self):
         self.pa.pa_write_kv(self.cache, self.k_new, self.v_new, self.slots, self.err)
 
     def decode(self):
+        if not self.nd:  # a step with no decoding sequence (spec-verify)
+            return
         self.pa.pa_decode(self.cache, self.out_dec, self.q_dec, self.tables_dec, self.lens_dec,
                           self.sm, self.w.window, self.ws, self.err)
 
@@ -202,6 +205,19 @@ def prefill_flops(w):
         pos = np.arange(L - C, L, dtype=np.int64)
         keys = np.minimum(pos + 1, w.window) if w.window > 0 else pos + 1
         total += int(keys.sum()) * w.num_q_heads * 4 * w.head_dim
+    return total
+
+
+def prefill_kv_bytes(w):
+    """Algorithmic KV bytes of the prefill call: each chunk's visible keys once per
+    kv head (the chunk's last query sees the most)."""
+    el = 1 if w.cache_dtype == "i8" else 2
+    per_tok = 2 * w.head_dim * el + (8 if w.cache_dtype == "i8" else 0)
+    total = 0
+    for b in range(w.num_decode, w.num_seqs):
+        L, C = int(w.context_lens[b]), int(w.q_lens[b])
+        lo = max(0, L - C - w.window + 1) if w.window > 0 else 0
+        total += (L - lo) * per_tok * w.num_kv_heads
     return total
 
 
@@ -311,9 +327,9 @@ def time_ours(args, w, torch, pa, I, rank, world):
 
 class OracleSample:
     """The CPU oracle as it stands (single-threaded C) on a bounded sample of the
-    workload: the first few decoding sequences, each in its own small pool.  One
-    run = the write of the sequence's new token + fp64 attention of its query,
-    on the first ``heads`` kv heads (and their GQA query heads)."""
+    workload: the first few sequences, each in its own small pool.  One run =
+    the write of the sequence's new tokens + fp64 attention of its queries, on
+    the first ``heads`` kv heads (and their GQA query heads)."""
 
     def __init__(self, w, I, nseq):
         import oracle
@@ -321,15 +337,16 @@ class OracleSample:
         self.per_tok = 2 * w.head_dim * (1 if w.cache_dtype == "i8" else 2) + (
             8 if w.cache_dtype == "i8" else 0)
         self.seqs = []
-        for b in range(min(nseq, w.num_decode)):
-            L = int(w.context_lens[b])
+        for b in range(min(nseq, w.num_seqs)):
+            L, C = int(w.context_lens[b]), int(w.q_lens[b])
             nblk = -(-L // w.block_size)
             c = oracle.Cache(w.cache_dtype, nblk, w.num_kv_heads, w.head_dim)
             kh, vh = I.history_rows(w, [b])
             slots = np.arange(L, dtype=np.int32)
-            oracle.write_kv(c, kh[:-1], vh[:-1], I.source_dtype(w), slots[:-1], lib=self.lib)
-            self.seqs.append(dict(L=L, nblk=nblk, cache=c, k=kh[-1:], v=vh[-1:], slot=slots[-1:],
-                                  q=I.query_rows(w, [b]), subs={}))
+            oracle.write_kv(c, kh[:L - C], vh[:L - C], I.source_dtype(w), slots[:L - C],
+                            lib=self.lib)
+            self.seqs.append(dict(L=L, C=C, nblk=nblk, cache=c, k=kh[L - C:], v=vh[L - C:],
+                                  slot=slots[L - C:], q=I.query_rows(w, [b]), subs={}))
         self.src = I.source_dtype(w)
 
     def run(self, i, heads=None):
@@ -347,14 +364,14 @@ class OracleSample:
         c, k, v, q = sq["subs"][heads]
         table = np.full((1, w.max_blocks_per_seq), -1, np.int32)
         table[0, :sq["nblk"]] = np.arange(sq["nblk"])
-        L = sq["L"]
+        L, C = sq["L"], sq["C"]
         t0 = time.perf_counter()
         o.write_kv(c, k, v, self.src, sq["slot"], lib=self.lib)
-        o.attention(c, q, w.q_dtype, np.array([0, 1], np.int32), table,
+        o.attention(c, q, w.q_dtype, np.array([0, C], np.int32), table,
                     np.array([L], np.int32), window=w.window, lib=self.lib)
         dt = time.perf_counter() - t0
-        eff = min(L, w.window) if w.window > 0 else L
-        return eff * self.per_tok * heads, dt
+        lo = max(0, L - C - w.window + 1) if w.window > 0 else 0
+        return (L - lo) * self.per_tok * heads, dt
 
 
 def cpu_baseline(w, I, budget_s, nseq=8):
@@ -393,7 +410,8 @@ def main():
            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
            "head_dim": w.head_dim, "block_size": w.block_size, "cache_dtype": w.cache_dtype,
            "q_dtype": w.q_dtype, "window": w.window, "num_blocks": w.num_blocks,
-           "mean_context": float(w.context_lens[:w.num_decode].mean()),
+           "mean_context": float(w.context_lens[:w.num_decode].mean() if w.num_decode
+                                 else w.context_lens.mean()),
            "kv_bytes_per_step": w.kv_bytes(),
            "l2": "inputs larger than L2" if w.kv_bytes() > 4 * L2_BYTES else
            "inputs smaller than L2 (not flushed)"}
@@ -415,8 +433,8 @@ def main():
             if i >= args.warmup:
                 rates.append(b / dt)
         value = statistics.median(rates) / 1e9
-        sample = ("per step: one of %d decoding sequences (whole context), %d of %d kv heads: "
-                  "write of the new token + fp64 attention" % (len(smp.seqs), heads,
+        sample = ("per step: one of the first %d sequences (whole context), %d of %d kv heads: "
+                  "write of its new tokens + fp64 attention of its queries" % (len(smp.seqs), heads,
                                                                 w.num_kv_heads))
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -449,14 +467,25 @@ def main():
     peaks, peak_kind = measured_peaks()
     dec_ms, pre_ms = statistics.mean(r["dec_ms"]), statistics.mean(r["pre_ms"])
     src = peak_kind + " (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
-    if pre_ms > dec_ms:  # the prefill kernel dominates: tensor-core roofline
-        flops = prefill_flops(w)
-        achieved = flops / (pre_ms * 1e-3) / 1e12
+    pre_flops, pre_bytes = prefill_flops(w), prefill_kv_bytes(w)
+    balance = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)  # flop per byte
+    if pre_ms > dec_ms and pre_flops > balance * pre_bytes:
+        # the prefill kernel dominates and is a dense contraction: tensor-core roofline
+        achieved = pre_flops / (pre_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": recorded_traffic(w.name, "prefill"),
                 "kernel": ("pa_prefill_chunk (tcgen05.mma kind::f16, TMEM accumulators)"
                            if w.cache_dtype != "i8" else "pa_prefill_chunk (mma.sync m16n8k16)"),
                 "peak_source": src + " bf16_tflops (burst)"}
+    elif pre_ms > dec_ms:
+        # the prefill kernel dominates with few queries per key (verification of a
+        # few drafted tokens): it streams the cache, HBM roofline
+        achieved = pre_bytes / (pre_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name, "prefill"),
+                "kernel": "pa_prefill_chunk (%d queries per sequence)" % int(w.q_lens.max()),
+                "peak_source": src + " hbm_gbs"}
     else:
         achieved = decode_kv_bytes(w) / (dec_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -481,9 +510,9 @@ def main():
         v, nseq, runs, spent = cpu_baseline(w, I, args.cpu_budget)
         line["cpu_baseline"] = {
             "value": v / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "%d runs over %d of %d decoding sequences (whole contexts, all heads): "
-                      "write of the new token + fp64 attention, %.1f s of CPU time"
-                      % (runs, nseq, w.num_decode, spent)}
+            "sample": "%d runs over the first %d of %d sequences (whole contexts, all heads): "
+                      "write of each one's new tokens + fp64 attention of its queries, "
+                      "%.1f s of CPU time" % (runs, nseq, w.num_seqs, spent)}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

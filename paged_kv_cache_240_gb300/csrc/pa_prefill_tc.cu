@@ -262,6 +262,22 @@ __device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsign
 __device__ __forceinline__ uint32_t sw_unit(int r, int u) {
   return (uint32_t)(r * 128 + (((u ^ r) & 7) << 4));
 }
+// Zero the V rows of block-start key `key0` (within a V stage) from row
+// `valid_rows` on: slots past the context end, which were never written.  Split
+// over the 128 threads of query tile 0; the writes are made visible to the
+// tensor core's (async proxy) reads.
+template <class LY>
+__device__ __forceinline__ void zero_v_tail(uint8_t* vbase, int key0, int valid_rows, int stid) {
+  const int nz = (kBlock - valid_rows) * LY::kChunks * 8;
+  for (int idx = stid; idx < nz; idx += kSoftmaxThreads) {
+    const int key = key0 + valid_rows + idx / (LY::kChunks * 8);
+    const int rest = idx % (LY::kChunks * 8);
+    *reinterpret_cast<uint4*>(vbase + (rest / 8) * LY::kKVChunk + sw_unit(key, rest % 8)) =
+        make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async();
+}
+
 // One work item: 256 query rows (two tiles) of one sequence's chunk and one kv
 // head, and the key range those rows can see.
 struct Item {
@@ -543,9 +559,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dV0 = sw128_desc(smem_u32(smem + LY::kVOff), LY::kKVChunk, 1024);
       bool started0 = false, started1 = false;  // O_q holds this item's first product
       // O_q (+)= P_q V of tile gg, skipping the blocks that were not loaded
+      bool live1 = true;  // query tile 1 of the current item has rows (short chunks may not)
       auto pv = [&](int q, int gg, bool& started) -> bool {
         if (!warp_wait(&p_full[q], gg & 1)) return false;
         fence_after();
+        if (q == 1 && !live1) {  // nothing to compute; the commit keeps the phases
+          commit_elect(&pv_done[q]);
+          return true;
+        }
         const uint64_t dV = dV0 + (uint64_t)(((gg % kVS) * LY::kKVBytes) >> 4);
         const uint32_t mask = bmask[gg % kFlagRing];
         const uint32_t dO = tmem + q * LY::kTileCols + LY::kOCol;
@@ -570,6 +591,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto s_mma = [&](int q, int gg, uint64_t dK) -> bool {
         if (gg >= 1 && !warp_wait(&pv_done[q], (gg - 1) & 1)) return false;
         fence_after();
+        if (q == 1 && !live1) {
+          commit_elect(&s_full[q]);
+          return true;
+        }
         const uint64_t dQ = dQ0 + (uint64_t)((q * LY::kQBytes) >> 4);
         const uint32_t dS = tmem + q * LY::kTileCols + LY::kSCol;
 #pragma unroll
@@ -590,6 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = warp_wait(q_full, k & 1);
         k++;
         started0 = started1 = false;
+        live1 = it.R0 + kRows < it.nrows;
         // Per tile g: P V of tile g-1 and S of tile g for each query tile, in the
         // order P V_0, S_0, P V_1, S_1, except that P V_1 goes first when its P is
         // already there, so the tensor pipe always has queued work while the MMA
@@ -655,9 +681,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u = 0; u < D / 8; u++) reinterpret_cast<uint4*>(dst)[u] = make_uint4(0, 0, 0, 0);
         continue;
       }
+      // a warp whose 32 rows are all past the chunk (short chunks) only keeps
+      // the barriers stepping and clears its share of the V tail
+      const bool warp_live = __any_sync(0xffffffffu, rvalid);
       // the block holding position L-1 may carry unwritten slots past it
       const int tail_blk = (it.L - 1) / kBlock;
       const int tail_rows = it.L % kBlock;  // valid rows of that block (0: all 16)
+      if (!warp_live) {
+        for (int t = 0; t < it.ntiles; t++, g++) {
+          if (!mbar_wait(&s_full[q], g & 1)) {
+            timed_out = true;
+            break;
+          }
+          fence_after();
+          const int blk0 = it.first + kTileBlocks * t;
+          const uint32_t mask = bmask[g % kFlagRing];
+          if (q == 0 && tail_rows != 0 && tail_blk >= blk0 && tail_blk < blk0 + kTileBlocks &&
+              ((mask >> (tail_blk - blk0)) & 1u)) {
+            if (!mbar_wait(&v_full[g % kVS], (g / kVS) & 1)) {
+              timed_out = true;
+              break;
+            }
+            zero_v_tail<LY>(smem + LY::kVOff + (g % kVS) * LY::kKVBytes,
+                            (tail_blk - blk0) * kBlock, tail_rows, stid);
+          }
+          fence_before();
+          mbar_arrive(&p_full[q]);
+        }
+        continue;
+      }
       float m_used = kNoMax, l = 0.0f;
       for (int t = 0; t < it.ntiles; t++, g++) {
         if (!mbar_wait(&s_full[q], g & 1)) {
@@ -675,8 +727,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // maximum of the scaled scores this row can see; an inner tile (every key
         // visible to every row of the warp) skips the masks.  Eight partial maxima
         // (three-input max) keep the dependency chains short.
-        const bool inner = __all_sync(0xffffffffu, (mask & 0xFFu) == 0xFFu && pos0 >= row_lo &&
-                                                       pos0 + kKeys - 1 <= row_hi) &&
+        // (rows past the chunk do not hold it back: their outputs are not stored,
+        // and each row of O depends on its own row of P only)
+        const bool inner = __all_sync(0xffffffffu, !rvalid || ((mask & 0xFFu) == 0xFFu &&
+                                                               pos0 >= row_lo &&
+                                                               pos0 + kKeys - 1 <= row_hi)) &&
                            sc > 0.0f;
         if (!inner) {
 #pragma unroll
@@ -748,15 +803,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             timed_out = true;
             break;
           }
-          uint8_t* vbase = smem + LY::kVOff + (g % kVS) * LY::kKVBytes;
-          const int nz = (kBlock - tail_rows) * LY::kChunks * 8;
-          for (int idx = stid; idx < nz; idx += kSoftmaxThreads) {
-            const int key = (tail_blk - blk0) * kBlock + tail_rows + idx / (LY::kChunks * 8);
-            const int rest = idx % (LY::kChunks * 8);
-            *reinterpret_cast<uint4*>(vbase + (rest / 8) * LY::kKVChunk + sw_unit(key, rest % 8)) =
-                make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async();
+          zero_v_tail<LY>(smem + LY::kVOff + (g % kVS) * LY::kKVBytes,
+                          (tail_blk - blk0) * kBlock, tail_rows, stid);
         }
         fence_before();
         mbar_arrive(&p_full[q]);

@@ -13,6 +13,7 @@ Workloads, shaped like the pages' (see the recipes in ``RECIPES``):
     block tables, chunked prefill sharing a step with decode.
   * "MicroGen", Key Features: dynamic INT8 KV quantisation, sliding window, GQA.
   * "llminfer", "Paged KV Cache And Continuous Batching": 16-token pages.
+  * "llminfer", Speculative Decoding: a verification pass over 8 drafted tokens.
 
 Every sequence's history (all positions before and including its new tokens) is
 drawn as K/V rows ~N(0, 1).  A cache is built by writing that history through a
@@ -45,6 +46,16 @@ RECIPES = {
     "int8-kv": dict(num_seqs=128, lens=("lognormal", 2048, 1.0, 8192), num_q_heads=32,
                     num_kv_heads=8, head_dim=128, cache_dtype="i8", q_dtype="bf16",
                     max_context=8192, window=0),
+    # Speculative-decode verification ("llminfer", Speculative Decoding: a
+    # Qwen2.5-1.5B target checking 8 assistant tokens; "PyTorch LLM Serving
+    # Engine", What is implemented: one target verification pass per proposal
+    # block): every sequence attends 9 new positions (the last accepted token and
+    # 8 drafts) over its paged history, causally among themselves.  256 sequences,
+    # prior context clipped log-normal around 2048.
+    "spec-verify": dict(num_seqs=0, lens=("fixed", []), num_q_heads=12, num_kv_heads=2,
+                        head_dim=128, cache_dtype="bf16", q_dtype="bf16", max_context=8192,
+                        window=0, num_chunks=256, chunk_len=9,
+                        prior=("lognormal", 2048, 1.0, 8192 - 9)),
     # 32 decode sequences plus 4 prefill chunks of 512 queries whose prior
     # context P0 ~ U[0, 3584] (so P0 + 512 <= 4096); sliding window 2048.
     "mixed": dict(num_seqs=32, lens=("uniform", 1, 4096), num_q_heads=32, num_kv_heads=8,
@@ -56,7 +67,8 @@ RECIPES = {
 @dataclasses.dataclass
 class Workload:
     """Bookkeeping of one step.  Sequences 0..num_decode-1 decode one token;
-    the rest (mixed workload only) each prefill one chunk of ``chunk_lens`` queries.
+    the rest (mixed and spec-verify workloads) each attend a chunk of ``q_lens``
+    new queries.
     ``context_lens`` count tokens after the step's write."""
     name: str
     num_q_heads: int
