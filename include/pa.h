@@ -67,7 +67,8 @@ typedef enum {
     PA_ERR_INVALID_ARG = 1,
     PA_ERR_UNSUPPORTED = 2,
     PA_ERR_CUDA = 3,
-    PA_ERR_DEVICE_DATA = 4
+    PA_ERR_DEVICE_DATA = 4,
+    PA_ERR_OUT_OF_BLOCKS = 5 /* pa_blocks.h: the pool has too few free blocks */
 } pa_status;
 
 typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_I8 = 2 } pa_dtype;

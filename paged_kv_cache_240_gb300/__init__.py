@@ -24,14 +24,19 @@ __all__ = [
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpa_gb300.so")
 
-PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_DEVICE_DATA = range(5)
+(PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_DEVICE_DATA,
+ PA_ERR_OUT_OF_BLOCKS) = range(6)
 PA_F16, PA_BF16, PA_I8 = 0, 1, 2
 PA_FLAG_SLOT_RANGE, PA_FLAG_BLOCK_ID, PA_FLAG_CONTEXT_LEN, PA_FLAG_Q_LEN, PA_FLAG_TIMEOUT = (
     1, 2, 4, 8, 16)
 
 EXPORTED_SYMBOLS = ("pa_write_kv", "pa_decode", "pa_decode_partitioned",
                     "pa_decode_workspace_bytes", "pa_decode_noalloc", "pa_prefill_chunk",
-                    "pa_status_str", "pa_last_cuda_error", "pa_check_flags")
+                    "pa_status_str", "pa_last_cuda_error", "pa_check_flags",
+                    "pa_blocks_create", "pa_blocks_destroy", "pa_blocks_append",
+                    "pa_blocks_rollback", "pa_blocks_release", "pa_blocks_preempt",
+                    "pa_blocks_evict_window", "pa_blocks_tables", "pa_blocks_context_len",
+                    "pa_blocks_get_stats")
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 

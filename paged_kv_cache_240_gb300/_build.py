@@ -1,5 +1,6 @@
 """Build the CUDA library in-tree: nvcc for sm_103a, one object per source in
-parallel, then one shared library with the C ABI of include/pa.h."""
+parallel, then one shared library with the C ABI of include/pa.h and
+include/pa_blocks.h."""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -21,7 +22,8 @@ FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", I
 
 
 def sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    """CUDA sources and host-only C++ sources (nvcc hands .cpp to the host compiler)."""
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():
@@ -43,7 +45,7 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     srcs = sources()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [NVCC, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

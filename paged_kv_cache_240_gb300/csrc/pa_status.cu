@@ -21,6 +21,7 @@ extern "C" const char* pa_status_str(pa_status status) {
     case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
     case PA_ERR_CUDA: return "PA_ERR_CUDA";
     case PA_ERR_DEVICE_DATA: return "PA_ERR_DEVICE_DATA";
+    case PA_ERR_OUT_OF_BLOCKS: return "PA_ERR_OUT_OF_BLOCKS";
   }
   return "PA_ERR_UNKNOWN";
 }

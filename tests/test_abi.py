@@ -1,5 +1,5 @@
 """The C-ABI library builds, loads and exports every entry point include/pa.h
-declares; host-side argument checks reject bad calls before any launch (no GPU
+and include/pa_blocks.h declare; host-side argument checks reject bad calls before any launch (no GPU
 needed: these calls never reach CUDA)."""
 import ctypes
 import os
@@ -11,7 +11,7 @@ import pytest
 import paged_kv_cache_240_gb300 as pa
 from paged_kv_cache_240_gb300 import _build
 
-HEADER = os.path.join(_build.INCLUDE, "pa.h")
+HEADERS = [os.path.join(_build.INCLUDE, h) for h in ("pa.h", "pa_blocks.h")]
 
 
 @pytest.fixture(scope="module")
@@ -21,7 +21,7 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
 
