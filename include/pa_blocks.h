@@ -7,7 +7,8 @@
  * blocks, per-sequence block tables, an O(1) free-list allocator, memory
  * accounting, explicit recomputation counters after preemption) and "MicroGen",
  * "Key Features" (logical-to-physical block mapping; sliding window eviction;
- * KV cache state rollback when speculative tokens are rejected).
+ * KV cache state rollback when speculative tokens are rejected; "Prompt Prefix
+ * Caching": token sequence hashing with sub-sequence prefix lookup).
  *
  * Layout conventions are those of pa.h: position p of a sequence lives in the
  * physical block block_tables[seq][p / block_size] at offset p % block_size,
@@ -39,6 +40,9 @@ typedef struct {
     long long recompute_tokens;  /* tokens dropped by preemption, to be computed again */
     long long evicted_blocks;    /* blocks freed by sliding-window eviction */
     long long rolled_back_tokens;/* tokens dropped by pa_blocks_rollback */
+    long long published_blocks;  /* blocks registered under a prefix key */
+    long long prefix_hit_blocks; /* blocks attached from the prefix cache (not recomputed) */
+    int shared_blocks;           /* blocks currently held by more than one sequence */
 } pa_blocks_stats;
 
 /*
@@ -66,12 +70,13 @@ pa_status pa_blocks_append(pa_blocks *bm, int seq, int num_tokens, int32_t *slot
 
 /*
  * pa_blocks_rollback -- drop the last num_tokens positions of seq (rejected
- * speculative tokens).  Blocks left without any position go back to the free
- * list; the dropped slots keep their stale contents, which no attention call
- * reads once the context is shorter, and the next append overwrites.
- * PA_ERR_INVALID_ARG when num_tokens exceeds the context, or when blocks were
- * evicted and the window of the next query (at the shortened context length L2:
- * keys L2-W+1 .. L2) would reach into them.
+ * speculative tokens).  Blocks left without any position are released (see
+ * reference counts below); the dropped slots keep their stale contents, which no
+ * attention call reads once the context is shorter, and the next append
+ * overwrites.  PA_ERR_INVALID_ARG when num_tokens exceeds the context, when
+ * blocks were evicted and the window of the next query (at the shortened context
+ * length L2: keys L2-W+1 .. L2) would reach into them, or when L2 would end
+ * inside a block another sequence shares (the next append would write into it).
  */
 pa_status pa_blocks_rollback(pa_blocks *bm, int seq, int num_tokens);
 
@@ -104,6 +109,29 @@ int pa_blocks_evict_window(pa_blocks *bm, int seq, int oldest_query, int32_t *fr
  */
 pa_status pa_blocks_tables(const pa_blocks *bm, const int32_t *seqs, int n, int32_t *tables_out,
                            int32_t *context_lens_out);
+
+/*
+ * Prefix caching.  Physical blocks are reference counted: a block returns to the
+ * free list when the last sequence holding it lets it go (release, preempt,
+ * eviction, rollback).  Only full blocks are shared, so appends never write into
+ * a shared block and no copy is ever needed.
+ *
+ * pa_blocks_publish -- register the first n_blocks blocks of seq, which must be
+ * full (n_blocks * block_size <= its context) and not evicted, under the
+ * caller's content keys keys[0..n_blocks-1] (for block i, a hash of every token
+ * of the sequence up to the block's end, so that equal keys mean equal K/V).  A
+ * key already registered keeps its block.  A block leaves the registry when it
+ * is freed.
+ *
+ * pa_blocks_attach_prefix -- for an empty sequence seq, attach the longest run
+ * of registered blocks matching keys[0], keys[1], ... (stopping at the first key
+ * not registered, or at max_blocks_per_seq): the sequence's table starts with
+ * those blocks, each gaining a reference, and its context length becomes
+ * (blocks attached) * block_size.  Returns the number of blocks attached (0 when
+ * the first key misses), or -1 on a bad argument or a non-empty sequence.
+ */
+pa_status pa_blocks_publish(pa_blocks *bm, int seq, const uint64_t *keys, int n_blocks);
+int pa_blocks_attach_prefix(pa_blocks *bm, int seq, const uint64_t *keys, int n_blocks);
 
 /* Context length of seq, or -1 for a bad seq. */
 int pa_blocks_context_len(const pa_blocks *bm, int seq);

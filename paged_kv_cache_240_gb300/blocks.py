@@ -13,7 +13,9 @@ class _Stats(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int), ("free_blocks", ctypes.c_int),
                 ("live_seqs", ctypes.c_int), ("tokens_held", ctypes.c_longlong),
                 ("preemptions", ctypes.c_longlong), ("recompute_tokens", ctypes.c_longlong),
-                ("evicted_blocks", ctypes.c_longlong), ("rolled_back_tokens", ctypes.c_longlong)]
+                ("evicted_blocks", ctypes.c_longlong), ("rolled_back_tokens", ctypes.c_longlong),
+                ("published_blocks", ctypes.c_longlong), ("prefix_hit_blocks", ctypes.c_longlong),
+                ("shared_blocks", ctypes.c_int)]
 
 
 def _lib():
@@ -33,9 +35,13 @@ def _lib():
         lib.pa_blocks_tables.argtypes = [P, i32p, I, i32p, i32p]
         lib.pa_blocks_context_len.argtypes = [P, I]
         lib.pa_blocks_get_stats.argtypes = [P, ctypes.POINTER(_Stats)]
+        u64p = ctypes.POINTER(ctypes.c_uint64)
+        lib.pa_blocks_publish.argtypes = [P, I, u64p, I]
+        lib.pa_blocks_attach_prefix.argtypes = [P, I, u64p, I]
         for name in ("pa_blocks_append", "pa_blocks_rollback", "pa_blocks_release",
                      "pa_blocks_preempt", "pa_blocks_evict_window", "pa_blocks_tables",
-                     "pa_blocks_context_len", "pa_blocks_get_stats"):
+                     "pa_blocks_context_len", "pa_blocks_get_stats", "pa_blocks_publish",
+                     "pa_blocks_attach_prefix"):
             getattr(lib, name).restype = I
         lib._pa_blocks_ready = True
     return lib
@@ -104,6 +110,23 @@ class BlockManager:
         _check(self._lib.pa_blocks_tables(self._h, _i32p(seqs), seqs.size, _i32p(tab),
                                           _i32p(lens)), "pa_blocks_tables")
         return tab, lens
+
+    def publish(self, seq: int, keys):
+        """Register seq's first len(keys) (full) blocks under the given prefix keys."""
+        keys = np.ascontiguousarray(keys, np.uint64)
+        _check(self._lib.pa_blocks_publish(
+            self._h, seq, keys.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), keys.size),
+            "pa_blocks_publish")
+
+    def attach_prefix(self, seq: int, keys) -> int:
+        """Attach the longest run of registered blocks matching keys to the empty
+        sequence seq; returns how many blocks were attached."""
+        keys = np.ascontiguousarray(keys, np.uint64)
+        k = self._lib.pa_blocks_attach_prefix(
+            self._h, seq, keys.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), keys.size)
+        if k < 0:
+            raise PaError(1, "pa_blocks_attach_prefix")
+        return k
 
     def context_len(self, seq: int) -> int:
         n = self._lib.pa_blocks_context_len(self._h, seq)

@@ -3,11 +3,13 @@
 // blocks, per-sequence block tables, an O(1) free-list allocator, memory
 // accounting, recomputation counters after preemption; "MicroGen", Key
 // Features: logical-to-physical block mapping, sliding window eviction, KV
-// cache state rollback).  Plain C++ on the host; the C ABI is pa_blocks.h.
+// cache state rollback; "Prompt Prefix Caching": token sequence hashing with
+// sub-sequence prefix lookup).  Plain C++ on the host; the C ABI is pa_blocks.h.
 #include "pa_blocks.h"
 
 #include <algorithm>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 struct pa_blocks {
@@ -16,6 +18,10 @@ struct pa_blocks {
   std::vector<int32_t> tables;      // [max_seqs][max_blocks_per_seq], -1 = no block
   std::vector<int32_t> lens;        // context length per sequence
   std::vector<int32_t> first_kept;  // logical blocks below this were evicted
+  std::vector<int32_t> refs;        // sequences holding each block
+  std::vector<uint64_t> key_of;     // the prefix key a block is registered under
+  std::vector<uint8_t> keyed;       // whether it is registered
+  std::unordered_map<uint64_t, int32_t> registry;  // prefix key -> block
   pa_blocks_stats stats;
 
   int32_t* table(int seq) { return tables.data() + (size_t)seq * max_blocks_per_seq; }
@@ -26,7 +32,24 @@ struct pa_blocks {
   int blocks_for(long long tokens) const {
     return (int)((tokens + block_size - 1) / block_size);
   }
-  void push_free(int32_t b) { free_stack.push_back(b); }
+  int32_t pop_free() {
+    const int32_t b = free_stack.back();
+    free_stack.pop_back();
+    refs[b] = 1;
+    return b;
+  }
+  // One holder lets block b go; the last one returns it to the free list.
+  void push_free(int32_t b) {
+    if (--refs[b] > 0) {
+      if (refs[b] == 1) stats.shared_blocks--;
+      return;
+    }
+    if (keyed[b]) {
+      registry.erase(key_of[b]);
+      keyed[b] = 0;
+    }
+    free_stack.push_back(b);
+  }
   // Return logical blocks [from, to) of seq to the free list (skipping holes).
   void free_range(int seq, int from, int to) {
     int32_t* t = table(seq);
@@ -66,6 +89,9 @@ extern "C" pa_blocks* pa_blocks_create(int num_blocks, int block_size, int max_s
     bm->tables.assign((size_t)max_seqs * max_blocks_per_seq, -1);
     bm->lens.assign(max_seqs, 0);
     bm->first_kept.assign(max_seqs, 0);
+    bm->refs.assign(num_blocks, 0);
+    bm->key_of.assign(num_blocks, 0);
+    bm->keyed.assign(num_blocks, 0);
   } catch (...) {
     delete bm;
     return nullptr;
@@ -86,10 +112,7 @@ extern "C" pa_status pa_blocks_append(pa_blocks* bm, int seq, int num_tokens,
   if (need > bm->max_blocks_per_seq) return PA_ERR_UNSUPPORTED;
   if (need - have > (int)bm->free_stack.size()) return PA_ERR_OUT_OF_BLOCKS;
   int32_t* t = bm->table(seq);
-  for (int i = have; i < need; i++) {
-    t[i] = bm->free_stack.back();
-    bm->free_stack.pop_back();
-  }
+  for (int i = have; i < need; i++) t[i] = bm->pop_free();
   for (int k = 0; k < num_tokens; k++) {
     const long long p = L + k;
     slots_out[k] = (int32_t)(t[p / bm->block_size] * (long long)bm->block_size +
@@ -110,6 +133,11 @@ extern "C" pa_status pa_blocks_rollback(pa_blocks* bm, int seq, int num_tokens) 
   if (bm->first_kept[seq] > 0 &&
       (long long)L2 - bm->window + 1 < (long long)bm->first_kept[seq] * bm->block_size)
     return PA_ERR_INVALID_ARG;
+  // the next append would write into the block holding position L2
+  if (L2 % bm->block_size != 0 && num_tokens > 0) {
+    const int32_t b = bm->table(seq)[L2 / bm->block_size];
+    if (b >= 0 && bm->refs[b] > 1) return PA_ERR_INVALID_ARG;
+  }
   bm->free_range(seq, bm->blocks_for(L2), bm->blocks_for(bm->lens[seq]));
   if (L2 == 0 && num_tokens > 0) bm->stats.live_seqs--;
   bm->lens[seq] = L2;
@@ -169,6 +197,52 @@ extern "C" pa_status pa_blocks_tables(const pa_blocks* bm, const int32_t* seqs, 
     if (context_lens_out) context_lens_out[i] = bm->lens[seqs[i]];
   }
   return PA_OK;
+}
+
+extern "C" pa_status pa_blocks_publish(pa_blocks* bm, int seq, const uint64_t* keys,
+                                       int n_blocks) {
+  if (!bm || !bm->valid_seq(seq) || n_blocks < 0 || (n_blocks > 0 && !keys))
+    return PA_ERR_INVALID_ARG;
+  if ((long long)n_blocks * bm->block_size > bm->lens[seq] || n_blocks > bm->max_blocks_per_seq)
+    return PA_ERR_INVALID_ARG;
+  const int32_t* t = bm->table(seq);
+  for (int i = 0; i < n_blocks; i++)
+    if (t[i] < 0) return PA_ERR_INVALID_ARG;  // evicted
+  try {
+    for (int i = 0; i < n_blocks; i++) {
+      const int32_t b = t[i];
+      if (bm->keyed[b] || bm->registry.count(keys[i])) continue;
+      bm->registry.emplace(keys[i], b);
+      bm->key_of[b] = keys[i];
+      bm->keyed[b] = 1;
+      bm->stats.published_blocks++;
+    }
+  } catch (...) {
+    return PA_ERR_INVALID_ARG;  // out of host memory: the registry keeps what it has
+  }
+  return PA_OK;
+}
+
+extern "C" int pa_blocks_attach_prefix(pa_blocks* bm, int seq, const uint64_t* keys,
+                                       int n_blocks) {
+  if (!bm || !bm->valid_seq(seq) || n_blocks < 0 || (n_blocks > 0 && !keys)) return -1;
+  if (bm->lens[seq] != 0 || bm->first_kept[seq] != 0) return -1;
+  int32_t* t = bm->table(seq);
+  int k = 0;
+  for (; k < n_blocks && k < bm->max_blocks_per_seq; k++) {
+    const auto hit = bm->registry.find(keys[k]);
+    if (hit == bm->registry.end()) break;
+    const int32_t b = hit->second;
+    if (++bm->refs[b] == 2) bm->stats.shared_blocks++;
+    t[k] = b;
+  }
+  if (k > 0) {
+    bm->lens[seq] = k * bm->block_size;
+    bm->stats.live_seqs++;
+    bm->stats.tokens_held += (long long)k * bm->block_size;
+    bm->stats.prefix_hit_blocks += k;
+  }
+  return k;
 }
 
 extern "C" int pa_blocks_context_len(const pa_blocks* bm, int seq) {

@@ -19,12 +19,15 @@ def built():
     _build.build()
 
 
-def check_invariants(bm, nseq):
+def check_invariants(bm, nseq, shared_ok=False):
     tab, lens = bm.tables(np.arange(nseq))
     owned = tab[tab >= 0]
     st = bm.stats()
-    assert len(set(owned.tolist())) == owned.size, "a block in two places"
-    assert owned.size + st["free_blocks"] == st["num_blocks"]
+    distinct = len(set(owned.tolist()))
+    if not shared_ok:
+        assert distinct == owned.size, "a block in two places"
+    assert st["shared_blocks"] == owned.size - distinct or shared_ok
+    assert distinct + st["free_blocks"] == st["num_blocks"]
     assert st["tokens_held"] == int(lens.sum())
     assert st["live_seqs"] == int((lens > 0).sum())
     for s in range(nseq):
@@ -241,3 +244,36 @@ def test_random_operations_match_the_model(seed):
         tab, lens = check_invariants(bm, ns)
         assert lens.tolist() == m.lens
         assert tab.tolist() == m.tab
+
+
+def test_prefix_blocks_are_shared_and_reference_counted():
+    bm = BlockManager(num_blocks=12, block_size=16, max_seqs=4, max_blocks_per_seq=8)
+    bm.append(0, 50)                      # 3 full blocks + 2 tokens
+    tab0, _ = bm.tables([0])
+    keys = np.array([101, 202, 303], np.uint64)
+    with pytest.raises(pa.PaError):
+        bm.publish(0, np.array([1, 2, 3, 4], np.uint64))   # block 3 is not full
+    bm.publish(0, keys)
+    assert bm.stats()["published_blocks"] == 3
+    # a request with the same first two blocks, then a different third
+    assert bm.attach_prefix(1, np.array([101, 202, 999], np.uint64)) == 2
+    tab, lens = check_invariants(bm, 4, shared_ok=True)
+    assert lens[1] == 32 and (tab[1, :2] == tab0[0, :2]).all()
+    st = bm.stats()
+    assert st["shared_blocks"] == 2 and st["prefix_hit_blocks"] == 2
+    new = bm.append(1, 5)                 # its own tokens go to a new block
+    assert not np.isin(new // 16, tab0[0]).any()
+    with pytest.raises(pa.PaError):
+        bm.rollback(1, 5 + 3)             # would end inside a shared block
+    assert bm.attach_prefix(2, np.array([555], np.uint64)) == 0   # miss
+    with pytest.raises(pa.PaError):
+        bm.attach_prefix(1, keys)         # only an empty sequence can attach
+    free_before = bm.stats()["free_blocks"]
+    bm.release(0)                         # the shared blocks stay alive for sequence 1
+    st = bm.stats()
+    assert st["shared_blocks"] == 0 and st["free_blocks"] == free_before + 2
+    assert bm.attach_prefix(3, keys) == 2  # still registered: held by sequence 1
+    bm.release(1)
+    bm.release(3)                         # last holders gone: blocks and keys freed
+    assert bm.stats()["free_blocks"] == 12
+    assert bm.attach_prefix(2, keys) == 0

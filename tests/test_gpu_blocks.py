@@ -96,3 +96,66 @@ def test_evicted_blocks_are_never_read(dtype, olib):
     torch.cuda.synchronize()
     assert int(err[0].item()) == 0
     assert_close(outc.double().cpu().numpy(), refc, "chunk after eviction")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "i8-bf16"])
+def test_shared_prefix_blocks(dtype, olib):
+    """Prefix caching: a prompt's full blocks are published; two later requests
+    attach them (one all of them, one a prefix of them) and append their own
+    tokens; decode and a chunk over the shared blocks match the oracle."""
+    cache_dt, q_dt = (dtype.split("-") + [None])[:2]
+    q_dt = q_dt or cache_dt
+    src = "bf16" if cache_dt == "i8" else cache_dt
+    bm = BlockManager(64, BS, max_seqs=3, max_blocks_per_seq=16)
+    cache = pa.PagedCache(64, HKV, D, cache_dt)
+    cache_o = oracle.Cache(cache_dt, 64, HKV, D)
+    oracle_poison(cache_o, cache_dt)
+    if cache_dt == "i8":
+        cache.k.fill_(POISON_CODE), cache.v.fill_(POISON_CODE)
+        cache.k_scale.fill_(float("nan")), cache.v_scale.fill_(float("nan"))
+    else:
+        cache.k.fill_(float("nan")), cache.v.fill_(float("nan"))
+
+    def add(seq, n, stream):
+        slots = bm.append(seq, n)
+        _write(cache, cache_o, I.normal_bits((n, HKV, D), src, 5, stream),
+               I.normal_bits((n, HKV, D), src, 5, stream + 1), slots, src, olib)
+
+    add(0, 100, 10)                               # the shared prompt: 6 full blocks + 4
+    keys = np.arange(1000, 1006, dtype=np.uint64)
+    bm.publish(0, keys)
+    assert bm.attach_prefix(1, keys) == 6         # the whole prompt prefix
+    add(1, 30, 20)
+    assert bm.attach_prefix(2, np.concatenate([keys[:3], [77]]).astype(np.uint64)) == 3
+    add(2, 19, 30)
+    assert bm.stats()["shared_blocks"] == 6
+    for s in range(3):                            # one decode token each
+        add(s, 1, 40 + 2 * s)
+    tables, ctx = bm.tables(np.arange(3, dtype=np.int32))
+    assert ctx.tolist() == [101, 127, 68]
+    assert (tables[1, :6] == tables[0, :6]).all() and (tables[2, :3] == tables[0, :3]).all()
+    sm = 1.0 / np.sqrt(D)
+    Hq = HKV * G
+    q = I.normal_bits((3, Hq, D), q_dt, 5, 4242)
+    ref = oracle.attention(cache_o, q, q_dt, np.arange(4, dtype=np.int32), tables, ctx,
+                           sm_scale=sm, window=0, lib=olib)
+    out = torch.empty((3, Hq, D), dtype=TORCH_DT[q_dt], device="cuda")
+    nbytes = pa.pa_decode_workspace_bytes(3, Hq, HKV, D, tables.shape[1], 0)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+    err = new_err()
+    pa.pa_decode(cache, out, bits_to_torch(q, q_dt), i32(tables), i32(ctx), sm, 0, ws, err)
+    torch.cuda.synchronize()
+    assert int(err[0].item()) == 0
+    assert_close(out.double().cpu().numpy(), ref, "decode over shared blocks")
+    # a chunk of the last 12 positions of sequence 1, over the shared prompt
+    t1, c1 = bm.tables(np.array([1], np.int32))
+    qc = I.normal_bits((12, Hq, D), q_dt, 5, 4343)
+    cu = np.array([0, 12], np.int32)
+    refc = oracle.attention(cache_o, qc, q_dt, cu, t1, c1, sm_scale=sm, window=0, lib=olib)
+    outc = torch.empty((12, Hq, D), dtype=TORCH_DT[q_dt], device="cuda")
+    err = new_err()
+    pa.pa_prefill_chunk(cache, outc, bits_to_torch(qc, q_dt), i32(cu), 12, i32(t1), i32(c1), sm,
+                        0, err)
+    torch.cuda.synchronize()
+    assert int(err[0].item()) == 0
+    assert_close(outc.double().cpu().numpy(), refc, "chunk over shared blocks")
