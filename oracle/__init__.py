@@ -69,6 +69,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pao_attention.argtypes = att + [P]
     lib.pao_attention_online.restype = i
     lib.pao_attention_online.argtypes = att + [i, P, i, P]
+    lib.pao_quantize_weights.argtypes = [i, P, i, i, P, P]
+    lib.pao_quantize_weights.restype = None
+    lib.pao_linear_int8.argtypes = [P, P, i, P, i, P, i, i, i, P]
+    lib.pao_linear_int8.restype = None
     _lib_cache[path] = lib
     return lib
 
@@ -184,6 +188,33 @@ def attention_online(cache: Cache, q_bits, q_dtype, cu_q_lens, block_tables,
     (lib or load()).pao_attention_online(*args, int(part_tokens), _ptr(seg), seg.size,
                                          _ptr(out))
     return out
+
+
+def quantize_weights(w_bits, w_dtype: str, lib=None):
+    """Per-output-channel int8 codes [n, k] and fp32 scales [n] of w [n, k]
+    (16-bit bit patterns); see ``pao_quantize_weights``."""
+    w = _c(w_bits, np.uint16)
+    n, k = w.shape
+    codes = np.zeros((n, k), np.int8)
+    scales = np.zeros(n, np.float32)
+    (lib or load()).pao_quantize_weights(DTYPES[w_dtype], _ptr(w), n, k, _ptr(codes),
+                                         _ptr(scales))
+    return codes, scales
+
+
+def linear_int8(codes, scales, x_bits, x_dtype: str, bias_bits=None, lib=None):
+    """y [m, n] (fp64) = x * (codes * scales)^T (+ bias); see ``pao_linear_int8``."""
+    codes = _c(codes, np.int8)
+    scales = _c(scales, np.float32)
+    x = _c(x_bits, np.uint16)
+    m, k = x.shape
+    n = codes.shape[0]
+    assert codes.shape == (n, k) and scales.shape == (n,)
+    y = np.zeros((m, n), np.float64)
+    bias = _c(bias_bits, np.uint16) if bias_bits is not None else np.zeros(1, np.uint16)
+    (lib or load()).pao_linear_int8(_ptr(codes), _ptr(scales), DTYPES[x_dtype], _ptr(x),
+                                    int(bias_bits is not None), _ptr(bias), m, n, k, _ptr(y))
+    return y
 
 
 def decode_cu_q_lens(num_seqs: int) -> np.ndarray:

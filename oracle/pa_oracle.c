@@ -421,3 +421,49 @@ int pao_attention_online(int cache_dtype, int num_blocks, int block_size,
     free(seg_s);
     return 0;
 }
+
+/*
+ * Weight-only INT8 linear layer ("PyTorch LLM Serving Engine", What is
+ * implemented: symmetric per-output-channel INT8 weights; "MicroGen", Key
+ * Features: static per-channel INT8 weight quantization).
+ *
+ * pao_quantize_weights: row n of w [n][k] (16-bit bit patterns, converted to
+ * fp32 exactly) is one output channel, quantised by pao_quantize_row (the rule
+ * of the INT8 KV rows: scale = amax/127, codes rounded half to even).
+ *
+ * pao_linear_int8: y[m][n] = sum_k x[m][k] * (code[n][k] * scale[n]) + bias[n],
+ * every term and the sum in fp64 (bias optional: has_bias = 0 leaves it out).
+ */
+void pao_quantize_weights(int w_dtype, const uint16_t *w, int n, int k, int8_t *codes,
+                          float *scales)
+{
+    float *row = (float *)malloc(sizeof(float) * (size_t)k);
+    if (!row)
+        return;
+    for (int i = 0; i < n; i++) {
+        for (int j = 0; j < k; j++) {
+            uint16_t b = w[(size_t)i * k + j];
+            row[j] = (float)(w_dtype == PAO_BF16 ? pao_bf16_to_double(b) : pao_f16_to_double(b));
+        }
+        pao_quantize_row(row, k, codes + (size_t)i * k, scales + i);
+    }
+    free(row);
+}
+
+void pao_linear_int8(const int8_t *codes, const float *scales, int x_dtype, const uint16_t *x,
+                     int has_bias, const uint16_t *bias, int m, int n, int k, double *y)
+{
+    for (int r = 0; r < m; r++) {
+        for (int i = 0; i < n; i++) {
+            double s = 0.0;
+            for (int j = 0; j < k; j++) {
+                uint16_t xb = x[(size_t)r * k + j];
+                double xv = x_dtype == PAO_BF16 ? pao_bf16_to_double(xb) : pao_f16_to_double(xb);
+                s += xv * ((double)codes[(size_t)i * k + j] * (double)scales[i]);
+            }
+            if (has_bias)
+                s += x_dtype == PAO_BF16 ? pao_bf16_to_double(bias[i]) : pao_f16_to_double(bias[i]);
+            y[(size_t)r * n + i] = s;
+        }
+    }
+}

@@ -36,7 +36,9 @@ EXPORTED_SYMBOLS = ("pa_write_kv", "pa_decode", "pa_decode_partitioned",
                     "pa_blocks_create", "pa_blocks_destroy", "pa_blocks_append",
                     "pa_blocks_rollback", "pa_blocks_release", "pa_blocks_preempt",
                     "pa_blocks_evict_window", "pa_blocks_tables", "pa_blocks_context_len",
-                    "pa_blocks_get_stats", "pa_blocks_publish", "pa_blocks_attach_prefix")
+                    "pa_blocks_get_stats", "pa_blocks_publish", "pa_blocks_attach_prefix",
+                    "pa_linear_int8_quantize", "pa_linear_int8_workspace_bytes",
+                    "pa_linear_int8")
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 

@@ -1,5 +1,5 @@
-"""The C-ABI library builds, loads and exports every entry point include/pa.h
-and include/pa_blocks.h declare; host-side argument checks reject bad calls before any launch (no GPU
+"""The C-ABI library builds, loads and exports every entry point include/pa.h,
+include/pa_blocks.h and include/pa_linear.h declare; host-side argument checks reject bad calls before any launch (no GPU
 needed: these calls never reach CUDA)."""
 import ctypes
 import os
@@ -11,7 +11,7 @@ import pytest
 import paged_kv_cache_240_gb300 as pa
 from paged_kv_cache_240_gb300 import _build
 
-HEADERS = [os.path.join(_build.INCLUDE, h) for h in ("pa.h", "pa_blocks.h")]
+HEADERS = [os.path.join(_build.INCLUDE, h) for h in ("pa.h", "pa_blocks.h", "pa_linear.h")]
 
 
 @pytest.fixture(scope="module")
@@ -23,7 +23,7 @@ def lib():
 def declared_functions():
     text = "".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_matches_binding():
@@ -33,7 +33,7 @@ def test_header_matches_binding():
 def test_library_exports_every_declared_symbol(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True,
                          text=True, check=True).stdout
-    exported = set(re.findall(r"\bT (pa_[a-z_]+)\b", out))
+    exported = set(re.findall(r"\bT (pa_[a-z0-9_]+)\b", out))
     for name in declared_functions():
         assert name in exported, name
         assert hasattr(lib, name)
