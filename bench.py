@@ -37,7 +37,8 @@ METRIC = "paged-attn decode KV-read GB/s (% of GB300 HBM peak); decode steps/sec
 DEFAULT_WORKLOAD = "mha-7b"
 L2_BYTES = 129 * 2 ** 20
 TRAFFIC_FILES = {"decode": os.path.join(ROOT, "profiles", "decode_traffic.json"),
-                 "prefill": os.path.join(ROOT, "profiles", "prefill_traffic.json")}
+                 "prefill": os.path.join(ROOT, "profiles", "prefill_traffic.json"),
+                 "linear": os.path.join(ROOT, "profiles", "linear_traffic.json")}
 
 
 def kernel_source_hash(files) -> str:
@@ -384,6 +385,176 @@ def cpu_baseline(w, I, budget_s, nseq=8):
     return nbytes / spent, len(smp.seqs), runs, spent
 
 
+# ------------------------------------------------------------------ INT8 linear
+
+# Four 7B-shaped decoder layers' projections (n output channels, k inputs):
+# q, k, v, o 4096x4096, gate and up 11008x4096, down 4096x11008 -- 810 MB of int8
+# codes, over six times the L2, so every step streams the weights from HBM.
+LINEAR_LAYERS = 4
+LINEAR_SHAPES = [(4096, 4096)] * 4 + [(11008, 4096)] * 2 + [(4096, 11008)]
+LINEAR_METRIC = "weight-only INT8 linear: weight-read GB/s (% of GB300 HBM peak)"
+
+
+def linear_bytes(m, shapes):
+    """Algorithmic bytes of one pass: every code and scale once, the activations
+    in and the outputs out (16-bit)."""
+    return sum(n * k + 4 * n + 2 * m * k + 2 * m * n for n, k in shapes)
+
+
+class OracleLinearSample:
+    """The oracle's INT8 linear (single-threaded C, fp64) on one 4096x4096 layer
+    with the same token count: a bounded sample of the workload."""
+
+    def __init__(self, m, I):
+        import oracle
+        self.oracle, self.lib, self.m = oracle, oracle.load(), m
+        n = k = 4096
+        rng = np.random.default_rng(7)
+        self.codes = rng.integers(-127, 128, size=(n, k), dtype=np.int8)
+        self.scales = (rng.random(n, dtype=np.float32) * 0.01 + 0.001).astype(np.float32)
+        self.x = I.normal_bits((m, k), "bf16", 7, 1)
+        self.bytes = linear_bytes(m, [(n, k)])
+
+    def run(self):
+        t0 = time.perf_counter()
+        self.oracle.linear_int8(self.codes, self.scales, self.x, "bf16", lib=self.lib)
+        return self.bytes, time.perf_counter() - t0
+
+
+def bench_linear(args):
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    m = args.num_seqs or 8
+    shapes = LINEAR_SHAPES * LINEAR_LAYERS
+    step_bytes = linear_bytes(m, shapes)
+    cfg = {"workload": "int8-linear", "tokens": m, "layers": LINEAR_LAYERS,
+           "shapes_n_k": LINEAR_SHAPES, "weight_bytes": sum(n * k for n, k in shapes),
+           "activation_dtype": "bf16", "l2": "inputs larger than L2"}
+    from paged_kv_cache_240_gb300 import inputs as I
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+        oracle.build()
+        smp = OracleLinearSample(m, I)
+        rates = []
+        for i in range(args.warmup + args.steps):
+            b, dt = smp.run()
+            if i >= args.warmup:
+                rates.append(b / dt)
+        value = statistics.median(rates) / 1e9
+        print(json.dumps({
+            "impl": "reference", "metric": LINEAR_METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_bytes / (value * 1e9) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": cfg,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "per step: one 4096x4096 layer, %d tokens" % m},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}))
+        return
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    from __graft_entry__ import build
+    build()
+    from paged_kv_cache_240_gb300 import linear as L
+    gen = torch.Generator(device="cuda").manual_seed(args.seed + 1000 * rank)
+    mats = []
+    for n, k in shapes:
+        codes = torch.randint(-127, 128, (n, k), dtype=torch.int8, device="cuda", generator=gen)
+        scales = torch.rand(n, device="cuda", generator=gen) * 0.01 + 0.001
+        x = torch.randn((m, k), device="cuda", generator=gen).to(torch.bfloat16)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+        mats.append((codes, scales, x, y))
+    nbytes = max(L.int8_workspace_bytes(m, n, k) for n, k in shapes)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+    launches = sum(1 + (1 if L.int8_workspace_bytes(m, n, k) else 0) for n, k in shapes)
+    stream = torch.cuda.Stream()
+
+    def step():
+        for codes, scales, x, y in mats:
+            L.int8_linear(codes, scales, x, out=y, workspace=ws)
+
+    run = capture(torch, step, stream).replay if not args.no_graph else step
+    try:
+        uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            run()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        clocks.start()
+        time.sleep(0.3)
+        step_ms = time_replays(torch, stream, run, args.steps)
+        if world > 1:
+            torch.distributed.barrier()
+        clk = clocks.stop()
+        # end to end: every layer's activations in from pinned memory, outputs back
+        hx = [x.cpu().pin_memory() for _, _, x, _ in mats]
+        hy = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _, _, _, y in mats]
+        h2d = sum(t.numel() * t.element_size() for t in hx)
+        d2h = sum(t.numel() * t.element_size() for t in hy)
+        e2e_steps = max(3, min(args.steps, 100))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for _ in range(e2e_steps):
+            for (_, _, x, _), t in zip(mats, hx):
+                x.copy_(t, non_blocking=True)
+            run()
+            for (_, _, _, y), t in zip(mats, hy):
+                t.copy_(y, non_blocking=True)
+        s1.record(stream)
+        torch.cuda.synchronize()
+    total_ms = sum(step_ms)
+    e2e_ms = s0.elapsed_time(s1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_ms], device="cuda", dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+    ms_per_step = total_ms / args.steps
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    peaks, peak_kind = measured_peaks()
+    src = peak_kind + " (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
+    achieved = step_bytes / (statistics.median(step_ms) * 1e-3) / 1e9
+    line = {"metric": LINEAR_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i8xbf16",
+            "data": "synthetic (random int8 codes and bf16 activations)", "config": cfg,
+            "clocks": clk,
+            "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches * args.steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic("int8-linear", "linear"),
+                         "kernel": "pa_linear_int8 (int8 codes -> exact f16, mma.sync m16n8k16)",
+                         "peak_source": src + " hbm_gbs"},
+            "p10_p50_p90_step_ms": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)]}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        smp = OracleLinearSample(m, I)
+        nb, spent, runs = 0, 0.0, 0
+        while spent < args.cpu_budget:
+            b, dt = smp.run()
+            nb, spent, runs = nb + b, spent + dt, runs + 1
+        line["cpu_baseline"] = {"value": nb / spent / 1e9, "unit": "GB/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": "%d runs of one 4096x4096 layer with %d tokens, %.1f s"
+                                          % (runs, m, spent)}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 # ------------------------------------------------------------------ main
 
 def main():
@@ -402,6 +573,9 @@ def main():
                     help="fewer decoding sequences (small profiling captures)")
     args = ap.parse_args()
 
+    if args.workload == "int8-linear":
+        bench_linear(args)
+        return
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     from paged_kv_cache_240_gb300 import inputs as I
