@@ -38,9 +38,15 @@ def test_quantize_bit_exact(dtype, n, k, olib):
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("m,n,k", [(1, 16, 64), (3, 48, 192), (8, 64, 512), (13, 32, 256),
-                                   (16, 128, 1024), (40, 16, 64), (5, 4096, 4096)])
+                                   (16, 128, 1024), (40, 16, 64), (5, 4096, 4096),
+                                   (9, 80, 640), (2, 1008, 4672), (17, 336, 2048),
+                                   (4, 16, 65536), (3, 5120, 640), (11, 9728, 576)])
 @pytest.mark.parametrize("with_bias", [False, True])
 def test_linear_matches_oracle(dtype, m, n, k, with_bias, olib):
+    """Ragged shapes (n = 80, 1008, 336 against 16-channel tiles; k = 640, 4672,
+    576 against the 64-wide k blocks), token groups past 16, shapes whose
+    thread blocks split k (small n: the workspace's partial sums and the
+    reduce) and shapes that do not, and no workspace at all."""
     w = _weights(n, k, dtype, 3 * m + n + k)
     x = I.normal_bits((m, k), dtype, 11, m + n + k)
     bias = I.normal_bits((n,), dtype, 12, m + n + k) if with_bias else None
@@ -57,6 +63,31 @@ def test_linear_matches_oracle(dtype, m, n, k, with_bias, olib):
         assert y.dtype == TORCH_DT[dtype] and y.shape == (m, n)
         assert_close(y.double().cpu().numpy(), ref,
                      "%s m=%d n=%d k=%d ws=%s" % (dtype, m, n, k, workspace is not None))
+
+
+def test_linear_chain_shares_workspace(olib):
+    """A chain of calls of different shapes back to back on one stream, all
+    with one workspace (split and unsplit shapes mixed), repeated: every
+    result matches the oracle and repeats give the same bits."""
+    dtype = "bf16"
+    shapes = [(8, 4096, 4096), (8, 1024, 11008), (3, 2048, 1024), (8, 5120, 640),
+              (12, 9728, 576), (8, 4096, 4096)]
+    nbytes = max(L.int8_workspace_bytes(m, n, k) for m, n, k in shapes)
+    assert nbytes > 0                             # some of these calls split k
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    mats = []
+    for i, (m, n, k) in enumerate(shapes):
+        w = _weights(n, k, dtype, 100 + i)
+        x = I.normal_bits((m, k), dtype, 13, i)
+        codes, scales = L.int8_quantize(bits_to_torch(w, dtype))
+        mats.append((codes, scales, x, bits_to_torch(x, dtype)))
+    outs = [[L.int8_linear(c, s, xt, workspace=ws) for c, s, _, xt in mats] for _ in range(3)]
+    torch.cuda.synchronize()
+    for j, (c, s, x, _) in enumerate(mats):
+        ref = oracle.linear_int8(c.cpu().numpy(), s.cpu().numpy(), x, dtype, lib=olib)
+        assert_close(outs[0][j].double().cpu().numpy(), ref, "chain %d" % j)
+        for rep in (1, 2):
+            assert torch.equal(outs[rep][j], outs[0][j])
 
 
 def test_linear_rejects_bad_shapes_and_alignment():
