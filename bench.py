@@ -425,9 +425,10 @@ def bench_linear(args):
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     m = args.num_seqs or 8
-    shapes = LINEAR_SHAPES * LINEAR_LAYERS
+    layers = args.layers or LINEAR_LAYERS
+    shapes = LINEAR_SHAPES * layers
     step_bytes = linear_bytes(m, shapes)
-    cfg = {"workload": "int8-linear", "tokens": m, "layers": LINEAR_LAYERS,
+    cfg = {"workload": "int8-linear", "tokens": m, "layers": layers,
            "shapes_n_k": LINEAR_SHAPES, "weight_bytes": sum(n * k for n, k in shapes),
            "activation_dtype": "bf16", "l2": "inputs larger than L2"}
     from paged_kv_cache_240_gb300 import inputs as I
@@ -569,6 +570,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every call from Python instead of replaying a CUDA graph")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="int8-linear only: layers per step (default %d)" % LINEAR_LAYERS)
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="fewer decoding sequences (small profiling captures)")
     args = ap.parse_args()
