@@ -47,7 +47,8 @@ constexpr int kCtaRows = kQTiles * kRows;
 constexpr int kKeys = 128;      // keys per tile (MMA N of S, K of P V)
 constexpr int kTileBlocks = kKeys / kBlock;  // 8
 constexpr int kKS = 3;          // K stages
-constexpr int kVS = 2;          // V stages
+constexpr int kVS = 2;          // V stages (the key split adds a third, see Layout)
+constexpr int kVSMax = 3;
 constexpr int kFlagRing = 8;    // tiles whose block-validity masks are kept
 constexpr int kSoftmaxThreads = 128;  // per query tile
 constexpr int kThreads = 128 + kQTiles * kSoftmaxThreads;  // 12 warps, 3 warpgroups
@@ -74,11 +75,19 @@ struct Layout {
   static constexpr int kBarOff = kVOff + kVS * kKVBytes;
   // barriers: k_full[KS], k_free[KS], v_full[VS], v_free[VS], q_full, q_free,
   // then per query tile s_full, p_full, pv_done
-  static constexpr int kNumBars = 2 * kKS + 2 * kVS + 2 + 3 * kQTiles;
+  static constexpr int kNumBars = 2 * kKS + 2 * kVSMax + 2 + 3 * kQTiles + 2;
   static constexpr int kFlagOff = kBarOff + kNumBars * 8;  // block masks [kFlagRing]
   static constexpr int kTmemSlotOff = kFlagOff + kFlagRing * 4;
   static constexpr int kOrderOff = kTmemSlotOff + 16;  // work order [kMaxPlan] uint16
-  static constexpr int kUsed = kOrderOff + kMaxPlan * 2;
+  static constexpr int kXchOff = kOrderOff + kMaxPlan * 2;  // key split: slot 1's weight per row
+  static constexpr int kUsed = kXchOff + kRows * 4;
+  // key split: both slots read query tile 0, and tile 1's space is a third V
+  // stage (a V tile is exactly a Q tile: 128 rows of D 16-bit values)
+  static constexpr int kV2Off = kQOff + kQBytes;
+  static_assert(kKVBytes == kQBytes, "the third V stage fills query tile 1");
+  static __host__ __device__ constexpr int v_off(int s) {
+    return s < kVS ? kVOff + s * kKVBytes : kV2Off;
+  }
   static constexpr int kBytes = kUsed + 1024;  // room to align the base to 1024
   // tensor memory columns per query tile: S (P in its first 64), then O
   static constexpr uint32_t kSCol = 0, kOCol = kKeys;
@@ -187,6 +196,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 columns of this thread's TMEM lane (as tmem_ld32).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
 
 // 128 consecutive fp32 columns of this thread's TMEM lane, one load and one wait
@@ -355,7 +380,14 @@ struct WorkList {
 // same items; the tile counter g (and the item counter k for Q) runs on across
 // items, so each barrier keeps stepping one phase at a time, and the next
 // item's Q and first K/V tiles load while the current item's last tiles finish.
-template <int D, typename QT>
+//
+// KS (key split; an item of at most 128 rows): both query slots hold the same
+// rows (query tile 0) and take the item's key tiles alternately, slot t & 1
+// taking tile t, so that two S -> softmax -> P V chains are in flight at once;
+// each slot keeps its own running maximum, normaliser and O, and slot 0's
+// threads merge the two at the end of the item (reading slot 1's O from the
+// same tensor-memory lanes and its (m, l) from shared memory).
+template <int D, typename QT, bool KS>
 __global__ void __launch_bounds__(kThreads, 1)
     pa_prefill_tc_kernel(const __grid_constant__ AttnParams p,
                          const __grid_constant__ CUtensorMap tmk,
@@ -369,12 +401,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_full = bars;
   uint64_t* k_free = k_full + kKS;
   uint64_t* v_full = k_free + kKS;
-  uint64_t* v_free = v_full + kVS;
-  uint64_t* q_full = v_free + kVS;
+  uint64_t* v_free = v_full + kVSMax;
+  uint64_t* q_full = v_free + kVSMax;
   uint64_t* q_free = q_full + 1;
   uint64_t* s_full = q_free + 1;          // [kQTiles]: S_q of the current tile is in TMEM
   uint64_t* p_full = s_full + kQTiles;    // [kQTiles]: P_q is in TMEM (128 arrivals)
   uint64_t* pv_done = p_full + kQTiles;   // [kQTiles]: the P V that read P_q finished
+  uint64_t* merge_ready = pv_done + kQTiles;  // KS: slot 1's (m, l) are in shared memory
+  uint64_t* merge_done = merge_ready + 1;     // KS: slot 0 has read slot 1's O
+  float* xch = reinterpret_cast<float*>(smem + LY::kXchOff);
+  constexpr int VS = KS ? kVSMax : kVS;  // V stages in use
   uint32_t* bmask = reinterpret_cast<uint32_t*>(smem + LY::kFlagOff);  // loaded blocks per tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::kTmemSlotOff);
 
@@ -386,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&k_full[i], 1);
       mbar_init(&k_free[i], 1);
     }
-    for (int i = 0; i < kVS; i++) {
+    for (int i = 0; i < VS; i++) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_free[i], 1);
     }
@@ -397,6 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&p_full[q], kSoftmaxThreads);
       mbar_init(&pv_done[q], 1);
     }
+    mbar_init(merge_ready, kSoftmaxThreads);
+    mbar_init(merge_done, kSoftmaxThreads);
     fence_mbar_init();
   }
   if (warp == 1) {  // tensor memory: per query tile, S (P in its first half) and O
@@ -451,11 +489,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         uint8_t* qs = smem + LY::kQOff;
+        constexpr int kQLoad = KS ? 1 : kQTiles;  // key split: tile 0 only
         if (q_tma) {
           // box [128/G tokens][G heads][64 columns] = 128 rows of the tile
-          if (lane == 0) mbar_arrive_expect_tx(q_full, kQTiles * LY::kQBytes);
+          if (lane == 0) mbar_arrive_expect_tx(q_full, kQLoad * LY::kQBytes);
           __syncwarp();
-          if (lane < kQTiles * LY::kChunks) {
+          if (lane < kQLoad * LY::kChunks) {
             const int q = lane / LY::kChunks, h = lane % LY::kChunks;
             tma_load_3d(qs + q * LY::kQBytes + h * (kRows * 128), &tmq, 64 * h, it.kvh * G,
                         it.q0 + (it.R0 + q * kRows) / G, q_full);
@@ -463,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane != 0) mbar_arrive(q_full);
         } else {
           const QT* qg = static_cast<const QT*>(p.q);
-          for (int r = lane; r < kCtaRows; r += 32) {
+          for (int r = lane; r < kQLoad * kRows; r += 32) {
             const int R = it.R0 + r;
             const bool rv = R < it.nrows;
             const long long orow =
@@ -521,15 +560,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           gk++;
           // V of tile gv (= gk - 1)
-          const int vs = gv % kVS;
-          if (gv >= kVS && !warp_wait(&v_free[vs], ((gv / kVS) - 1) & 1)) {
+          const int vs = gv % VS;
+          if (gv >= VS && !warp_wait(&v_free[vs], ((gv / VS) - 1) & 1)) {
             timed_out = true;
             break;
           }
           if (lane == 0) mbar_arrive_expect_tx(&v_full[vs], tile_bytes);
           __syncwarp();
           if (ok) {
-            uint8_t* vbase = smem + LY::kVOff + vs * LY::kKVBytes;
+            uint8_t* vbase = smem + LY::v_off(vs);
 #pragma unroll
             for (int h = 0; h < LY::kChunks; h++)
               tma_load_2d(vbase + h * LY::kKVChunk + lane * kBlock * 128, &tmv, 64 * h, row0,
@@ -543,8 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         for (int t = gk > kKS ? gk - kKS : 0; t < gk; t++)
           if (!mbar_wait(&k_full[t % kKS], (t / kKS) & 1)) break;
-        for (int t = gv > kVS ? gv - kVS : 0; t < gv; t++)
-          if (!mbar_wait(&v_full[t % kVS], (t / kVS) & 1)) break;
+        for (int t = gv > VS ? gv - VS : 0; t < gv; t++)
+          if (!mbar_wait(&v_full[t % VS], (t / VS) & 1)) break;
         if (k > 0) mbar_wait(q_full, (k - 1) & 1);
       }
       if (timed_out && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
@@ -607,46 +646,119 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       static_assert(kQTiles == 2, "the MMA schedule is written for two query tiles");
       bool ok = true;
-      int g = 0, k = 0;
-      int n, kvh, tile;
-      for (int j = 0; ok && wl.at(j, n, kvh, tile); j++) {
-        const Item it = item_info(p, n, kvh, tile, false);
-        if (!it.valid || it.ntiles == 0) continue;
-        ok = warp_wait(q_full, k & 1);
-        k++;
-        started0 = started1 = false;
-        live1 = it.R0 + kRows < it.nrows;
-        // Per tile g: P V of tile g-1 and S of tile g for each query tile, in the
-        // order P V_0, S_0, P V_1, S_1, except that P V_1 goes first when its P is
-        // already there, so the tensor pipe always has queued work while the MMA
-        // warp waits for a P V to finish before the S that overwrites its P.
-        for (int t = 0; t < it.ntiles && ok; t++, g++) {
-          ok = warp_wait(&k_full[g % kKS], (g / kKS) & 1);
-          const uint64_t dK = dK0 + (uint64_t)(((g % kKS) * LY::kKVBytes) >> 4);
-          if (ok && t >= 1) {
+      if constexpr (KS) {
+        // slot q's tiles so far (c[q]) step its barriers; per tile: S into the
+        // tile's slot, then P V of the previous tile (the other slot)
+        // P V of tile gg into slot q (its c-th tile); returns whether O_q now holds
+        // a product, or -1 if the wait ran out
+        auto pvk = [&](int q, int c, int gg, bool started) -> int {
+          if (!warp_wait(&p_full[q], c & 1)) return -1;
+          fence_after();
+          const uint64_t dV = sw128_desc(smem_u32(smem + LY::v_off(gg % VS)), LY::kKVChunk, 1024);
+          const uint32_t mask = bmask[gg % kFlagRing];
+          const uint32_t dO = tmem + q * LY::kTileCols + LY::kOCol;
+          const uint32_t aP = tmem + q * LY::kTileCols + LY::kSCol;
+#pragma unroll
+          for (int s = 0; s < kTileBlocks; s++)
+            if ((mask >> s) & 1u) {
+              mma_elect_tmem_a(dO, aP + 8 * s, dV + (uint64_t)((2048 * s) >> 4), idO,
+                               started ? 1u : 0u);
+              started = true;
+            }
+          commit_elect(&pv_done[q]);
+          return started ? 1 : 0;
+        };
+        auto sk = [&](int q, int c, uint64_t dK) -> bool {
+          if (c >= 1 && !warp_wait(&pv_done[q], (c - 1) & 1)) return false;
+          fence_after();
+          const uint32_t dS = tmem + q * LY::kTileCols + LY::kSCol;
+#pragma unroll
+          for (int s = 0; s < D / 16; s++)
+            mma_elect(dS, dQ0 + (uint64_t)(((s / 4) * (kRows * 128) + (s % 4) * 32) >> 4),
+                      dK + (uint64_t)(((s / 4) * LY::kKVChunk + (s % 4) * 32) >> 4), idS,
+                      s > 0 ? 1u : 0u);
+          commit_elect(&s_full[q]);
+          return true;
+        };
+        int g = 0, k = 0, c0 = 0, c1 = 0;  // c_q: slot q's tiles so far
+        int n, kvh, tile;
+        for (int j = 0; ok && wl.at(j, n, kvh, tile); j++) {
+          const Item it = item_info(p, n, kvh, tile, false);
+          if (!it.valid || it.ntiles == 0) continue;
+          ok = warp_wait(q_full, k & 1);
+          k++;
+          bool st0 = false, st1 = false;  // O_q holds this item's first product
+          int pq = 0, pc = 0;             // slot and slot count of the previous tile
+          auto pv_prev = [&]() {
+            ok = warp_wait(&v_full[(g - 1) % VS], ((g - 1) / VS) & 1);
+            if (!ok) return;
+            const int r = pvk(pq, pc, g - 1, pq ? st1 : st0);
+            if (r < 0) {
+              ok = false;
+              return;
+            }
+            if (pq) st1 = r != 0;
+            else st0 = r != 0;
+            commit_elect(&v_free[(g - 1) % VS]);
+          };
+          for (int t = 0; t < it.ntiles && ok; t++, g++) {
+            const int q = t & 1;
+            const int cq = q ? c1 : c0;
+            ok = warp_wait(&k_full[g % kKS], (g / kKS) & 1);
+            const uint64_t dK = dK0 + (uint64_t)(((g % kKS) * LY::kKVBytes) >> 4);
+            if (ok) ok = sk(q, cq, dK);
+            if (ok) commit_elect(&k_free[g % kKS]);
+            if (ok && t == it.ntiles - 1) commit_elect(q_free);  // Q is no longer read
+            if (ok && t >= 1) pv_prev();
+            pq = q;
+            pc = cq;
+            if (q) c1++;
+            else c0++;
+          }
+          if (ok) pv_prev();  // the item's last tile
+        }
+      } else {
+        int g = 0, k = 0;
+        int n, kvh, tile;
+        for (int j = 0; ok && wl.at(j, n, kvh, tile); j++) {
+          const Item it = item_info(p, n, kvh, tile, false);
+          if (!it.valid || it.ntiles == 0) continue;
+          ok = warp_wait(q_full, k & 1);
+          k++;
+          started0 = started1 = false;
+          live1 = it.R0 + kRows < it.nrows;
+          // Per tile g: P V of tile g-1 and S of tile g for each query tile, in the
+          // order P V_0, S_0, P V_1, S_1, except that P V_1 goes first when its P is
+          // already there, so the tensor pipe always has queued work while the MMA
+          // warp waits for a P V to finish before the S that overwrites its P.
+          for (int t = 0; t < it.ntiles && ok; t++, g++) {
+            ok = warp_wait(&k_full[g % kKS], (g / kKS) & 1);
+            const uint64_t dK = dK0 + (uint64_t)(((g % kKS) * LY::kKVBytes) >> 4);
+            if (ok && t >= 1) {
+              ok = warp_wait(&v_full[(g - 1) % kVS], ((g - 1) / kVS) & 1);
+              if (ok) ok = pv(0, g - 1, started0);
+              bool pv1 = false;
+              if (ok && warp_test(&p_full[1], (g - 1) & 1)) {
+                ok = pv(1, g - 1, started1);
+                pv1 = true;
+              }
+              if (ok) ok = s_mma(0, g, dK);
+              if (ok && !pv1) ok = pv(1, g - 1, started1);
+              if (ok) commit_elect(&v_free[(g - 1) % kVS]);
+              if (ok) ok = s_mma(1, g, dK);
+            } else if (ok) {
+              ok = s_mma(0, g, dK);
+              if (ok) ok = s_mma(1, g, dK);
+            }
+            if (ok) commit_elect(&k_free[g % kKS]);
+            if (ok && t == it.ntiles - 1) commit_elect(q_free);  // Q is no longer read
+          }
+          if (ok) {  // the item's last tile
             ok = warp_wait(&v_full[(g - 1) % kVS], ((g - 1) / kVS) & 1);
             if (ok) ok = pv(0, g - 1, started0);
-            bool pv1 = false;
-            if (ok && warp_test(&p_full[1], (g - 1) & 1)) {
-              ok = pv(1, g - 1, started1);
-              pv1 = true;
-            }
-            if (ok) ok = s_mma(0, g, dK);
-            if (ok && !pv1) ok = pv(1, g - 1, started1);
+            if (ok) ok = pv(1, g - 1, started1);
             if (ok) commit_elect(&v_free[(g - 1) % kVS]);
-            if (ok) ok = s_mma(1, g, dK);
-          } else if (ok) {
-            ok = s_mma(0, g, dK);
-            if (ok) ok = s_mma(1, g, dK);
           }
-          if (ok) commit_elect(&k_free[g % kKS]);
-          if (ok && t == it.ntiles - 1) commit_elect(q_free);  // Q is no longer read
-        }
-        if (ok) {  // the item's last tile
-          ok = warp_wait(&v_full[(g - 1) % kVS], ((g - 1) / kVS) & 1);
-          if (ok) ok = pv(0, g - 1, started0);
-          if (ok) ok = pv(1, g - 1, started1);
-          if (ok) commit_elect(&v_free[(g - 1) % kVS]);
         }
       }
       if (!ok && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
@@ -662,11 +774,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sc = p.scale_log2;
     QT* out = static_cast<QT*>(p.out);
     int g = 0;
+    // KS: this slot's tiles so far (its barriers' phases), slot 1's tiles so far
+    // (slot 0 waits on its P V), and items merged so far
+    int cq = 0, c1 = 0, kk = 0;
     int n, kvh, tile;
     for (int j = 0; !timed_out && wl.at(j, n, kvh, tile); j++) {
       const Item it = item_info(p, n, kvh, tile, false);
       if (!it.valid) continue;
-      const int R = it.R0 + q * kRows + row;
+      const int R = it.R0 + (KS ? 0 : q * kRows) + row;
       const bool rvalid = R < it.nrows;
       const int c = rvalid ? R / G : 0;
       const int pos = it.L - it.C + c;
@@ -676,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           (long long)(it.q0 + c) * p.num_q_heads + it.kvh * G + (rvalid ? R % G : 0);
       QT* dst = out + orow * D;
       if (it.ntiles == 0) {  // no row sees a key: zeros
-        if (rvalid)
+        if (rvalid && (!KS || q == 0))
 #pragma unroll
           for (int u = 0; u < D / 8; u++) reinterpret_cast<uint4*>(dst)[u] = make_uint4(0, 0, 0, 0);
         continue;
@@ -687,35 +802,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the block holding position L-1 may carry unwritten slots past it
       const int tail_blk = (it.L - 1) / kBlock;
       const int tail_rows = it.L % kBlock;  // valid rows of that block (0: all 16)
+      const bool two = KS && it.ntiles >= 2;  // KS: slot 1 has tiles, the slots merge
       if (!warp_live) {
         for (int t = 0; t < it.ntiles; t++, g++) {
-          if (!mbar_wait(&s_full[q], g & 1)) {
+          if (KS && (t & 1) != q) continue;  // the other slot's tile
+          if (!mbar_wait(&s_full[q], (KS ? cq : g) & 1)) {
             timed_out = true;
             break;
           }
+          if (KS) cq++;
           fence_after();
           const int blk0 = it.first + kTileBlocks * t;
           const uint32_t mask = bmask[g % kFlagRing];
-          if (q == 0 && tail_rows != 0 && tail_blk >= blk0 && tail_blk < blk0 + kTileBlocks &&
-              ((mask >> (tail_blk - blk0)) & 1u)) {
-            if (!mbar_wait(&v_full[g % kVS], (g / kVS) & 1)) {
+          if ((KS || q == 0) && tail_rows != 0 && tail_blk >= blk0 &&
+              tail_blk < blk0 + kTileBlocks && ((mask >> (tail_blk - blk0)) & 1u)) {
+            if (!mbar_wait(&v_full[g % VS], (g / VS) & 1)) {
               timed_out = true;
               break;
             }
-            zero_v_tail<LY>(smem + LY::kVOff + (g % kVS) * LY::kKVBytes,
+            zero_v_tail<LY>(smem + LY::v_off(g % VS),
                             (tail_blk - blk0) * kBlock, tail_rows, stid);
           }
           fence_before();
           mbar_arrive(&p_full[q]);
         }
+        if (timed_out) break;
+        if (two) {  // the merge handshake, without data
+          if (q == 1) {
+            mbar_arrive(merge_ready);
+            if (!mbar_wait(merge_done, kk & 1)) timed_out = true;
+          } else {
+            if (!mbar_wait(merge_ready, kk & 1)) timed_out = true;
+            mbar_arrive(merge_done);
+          }
+          kk++;
+        }
+        if (KS && q == 0) c1 += it.ntiles / 2;
         continue;
       }
       float m_used = kNoMax, l = 0.0f;
       for (int t = 0; t < it.ntiles; t++, g++) {
-        if (!mbar_wait(&s_full[q], g & 1)) {
+        if (KS && (t & 1) != q) continue;  // the other slot's tile
+        if (!mbar_wait(&s_full[q], (KS ? cq : g) & 1)) {
           timed_out = true;
           break;
         }
+        if (KS) cq++;
         // S of tile g is complete, and with it (it was issued after waiting for
         // it) the P V of tile g-1: O holds every earlier tile
         fence_after();
@@ -784,8 +916,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // P over the first 64 columns of S (this thread's S values are all read)
         tmem_st64(lane_base + LY::kSCol, pk);
-        if (rescale && t > 0) {
-          // O holds this item's tiles < t (their P V is complete): scale it in place
+        if (rescale && t > (KS ? 1 : 0)) {
+          // O holds this item's earlier tiles (their P V is complete): scale it in place
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
             float v[32];
@@ -797,19 +929,106 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // unwritten slots past L-1 in a loaded block: zero their V rows, so that
         // 0 * V stays 0 (query tile 0's warps; the MMA warp waits for both tiles' P)
-        if (q == 0 && tail_rows != 0 && tail_blk >= blk0 && tail_blk < blk0 + kTileBlocks &&
-            ((mask >> (tail_blk - blk0)) & 1u)) {
-          if (!mbar_wait(&v_full[g % kVS], (g / kVS) & 1)) {
+        if ((KS || q == 0) && tail_rows != 0 && tail_blk >= blk0 &&
+            tail_blk < blk0 + kTileBlocks && ((mask >> (tail_blk - blk0)) & 1u)) {
+          if (!mbar_wait(&v_full[g % VS], (g / VS) & 1)) {
             timed_out = true;
             break;
           }
-          zero_v_tail<LY>(smem + LY::kVOff + (g % kVS) * LY::kKVBytes,
+          zero_v_tail<LY>(smem + LY::v_off(g % VS),
                           (tail_blk - blk0) * kBlock, tail_rows, stid);
         }
         fence_before();
         mbar_arrive(&p_full[q]);
       }
       if (timed_out) break;
+      if constexpr (KS) {
+        if (q == 1) {
+          // slot 1, if it had tiles: hand (m, l) to slot 0, which reads O_1; the
+          // next item's first P V into O_1 waits for this slot's next P
+          if (two) {
+            // O_1 / l_1 in place, and its weight log2(l_1) + m_1 for slot 0
+            if (!mbar_wait(&pv_done[1], (cq - 1) & 1)) {
+              timed_out = true;
+              break;
+            }
+            fence_after();
+            {
+              // the whole warp takes part in the tensor-memory copies (they are
+              // .sync.aligned); a row without weight is scaled by 0 and slot 0
+              // leaves it out by its weight
+              const float inv1 = l > 0.0f ? 1.0f / l : 0.0f;
+#pragma unroll
+              for (int c0 = 0; c0 < D; c0 += 32) {
+                float v[32];
+                tmem_ld32(lane_base + LY::kOCol + c0, v);
+#pragma unroll
+                for (int i = 0; i < 32; i++) v[i] *= inv1;
+                tmem_st32(lane_base + LY::kOCol + c0, v);
+              }
+            }
+            xch[row] = l > 0.0f ? m_used + __log2f(l) : kNoMax;
+            fence_before();
+            mbar_arrive(merge_ready);
+            if (!mbar_wait(merge_done, kk & 1)) {
+              timed_out = true;
+              break;
+            }
+            kk++;
+          }
+          continue;
+        }
+        c1 += it.ntiles / 2;
+        // slot 0: both slots' last P V, then O = (O_0 2^(m_0 - M) + O_1 2^(m_1 - M)) /
+        // (l_0 2^(m_0 - M) + l_1 2^(m_1 - M)), a slot without weight left out
+        if (!mbar_wait(&pv_done[0], (cq - 1) & 1) ||
+            (two && (!mbar_wait(merge_ready, kk & 1) || !mbar_wait(&pv_done[1], (c1 - 1) & 1)))) {
+          timed_out = true;
+          break;
+        }
+        fence_after();
+        // slot 1 left O_1 / l_1 and lam = log2(l_1) + m_1 (kNoMax: no weight), so
+        // O = (O_0 2^(m_0 - M) + (O_1 / l_1) 2^(lam - M)) / (l_0 2^(m_0 - M) + 2^(lam - M))
+        const float lam = two ? xch[row] : kNoMax;
+        const bool has1 = lam > 0.5f * kNoMax;
+        const float mM = fmaxf(l > 0.0f ? m_used : kNoMax, has1 ? lam : kNoMax);
+        const float f0 = l > 0.0f ? fast_exp2(m_used - mM) : 0.0f;
+        const float f1 = has1 ? fast_exp2(lam - mM) : 0.0f;
+        const float lt = l * f0 + f1;
+        const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+        const float w0 = f0 * inv, w1 = f1 * inv;
+        const uint32_t lane_base1 = lane_base + LY::kTileCols;  // slot 1, the same lanes
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          float v[16], v1[16];
+          tmem_ld16(lane_base + LY::kOCol + c0, v);
+          if (two) tmem_ld16(lane_base1 + LY::kOCol + c0, v1);
+          if (rvalid) {
+            float w[16];
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+              const float a0 = l > 0.0f ? v[i] * w0 : 0.0f;
+              const float a1 = has1 ? v1[i] * w1 : 0.0f;
+              w[i] = a0 + a1;
+            }
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+              uint4 o4;
+              o4.x = pack2<BF>(w[8 * u + 0], w[8 * u + 1]);
+              o4.y = pack2<BF>(w[8 * u + 2], w[8 * u + 3]);
+              o4.z = pack2<BF>(w[8 * u + 4], w[8 * u + 5]);
+              o4.w = pack2<BF>(w[8 * u + 6], w[8 * u + 7]);
+              *reinterpret_cast<uint4*>(dst + c0 + 8 * u) = o4;
+            }
+          }
+        }
+        fence_before();  // O's reads are ordered before the next item's first P V
+        if (two) {
+          mbar_arrive(merge_done);
+          kk++;
+        }
+        continue;
+      }
       // epilogue: wait for this item's last P V (tile g-1)
       if (!mbar_wait(&pv_done[q], (g - 1) & 1)) {
         timed_out = true;
@@ -882,11 +1101,11 @@ bool encode_q_map(CUtensorMap* m, const AttnParams& p, int D, bool bf16) {
 
 }  // namespace
 
-template <int D, typename QT>
-cudaError_t launch_prefill_tc(const AttnParams& p, const CUtensorMap& tmk,
-                              const CUtensorMap& tmv, int num_seqs, cudaStream_t stream) {
+template <int D, typename QT, bool KS>
+cudaError_t launch_prefill_tc_ks(const AttnParams& p, const CUtensorMap& tmk,
+                                 const CUtensorMap& tmv, int num_seqs, cudaStream_t stream) {
   constexpr int smem = tc::Layout<D>::kBytes;
-  auto kern = tc::pa_prefill_tc_kernel<D, QT>;
+  auto kern = tc::pa_prefill_tc_kernel<D, QT, KS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // setmaxnreg moves registers between warpgroups inside the CTA's launch
@@ -911,6 +1130,16 @@ cudaError_t launch_prefill_tc(const AttnParams& p, const CUtensorMap& tmk,
   const unsigned grid = (unsigned)std::min<long long>(items, sms);
   kern<<<grid, tc::kThreads, smem, stream>>>(pt, tmk, tmv, tmq, num_seqs, q_tma ? 1 : 0);
   return cudaGetLastError();
+}
+
+// Chunks of at most 128 query rows (a few queries per sequence, e.g. a draft
+// verification) take the key-split kernel: one query tile's rows in both slots.
+template <int D, typename QT>
+cudaError_t launch_prefill_tc(const AttnParams& p, const CUtensorMap& tmk,
+                              const CUtensorMap& tmv, int num_seqs, cudaStream_t stream) {
+  if ((long long)p.max_q_len * p.group <= tc::kRows)
+    return launch_prefill_tc_ks<D, QT, true>(p, tmk, tmv, num_seqs, stream);
+  return launch_prefill_tc_ks<D, QT, false>(p, tmk, tmv, num_seqs, stream);
 }
 
 template cudaError_t launch_prefill_tc<64, __half>(const AttnParams&, const CUtensorMap&,
