@@ -69,6 +69,31 @@ def test_verify_matches_oracle(dtype, G, D, window, olib):
     assert_close(got, ref, "verify %s G=%d D=%d W=%d" % (dtype, G, D, window))
 
 
+@pytest.mark.parametrize("dtype,G,D,window,C", [
+    ("bf16", 6, 128, 0, 9),     # 54 rows: both query slots on one tile's rows
+    ("f16", 4, 64, 0, 32),      # 128 rows: the largest chunk that does so
+    ("bf16", 4, 128, 0, 33),    # 132 rows: two query tiles, the second nearly empty
+    ("bf16", 6, 128, 200, 9),   # a sliding window
+])
+def test_short_chunk_key_tiles(dtype, G, D, window, C, olib):
+    """Chunks of a few queries over contexts chosen around the 128-key tiles:
+    one key tile (the second query slot of a one-tile chunk gets none), two
+    tiles, odd and even counts, and the context's partly written last block in
+    either slot's tile (L = 9, 100, 128, 129, 200, 256, 257, 300, 383, 384, 520,
+    1000, 1037)."""
+    ctx = [9, 100, 128, 129, 200, 256, 257, 300, 383, 384, 520, 1000, 1037]
+    w = I.make_workload("spec-verify", seed=90 + C + G, num_seqs=len(ctx), lens=("fixed", ctx),
+                        num_chunks=0, window=window)
+    cache_dt, q_dt = (dtype.split("-") + [None])[:2]
+    w.cache_dtype, w.q_dtype = cache_dt, q_dt or cache_dt
+    w.num_kv_heads, w.num_q_heads, w.head_dim = 2, 2 * G, D
+    w.q_lens = np.minimum(C, w.context_lens).astype(np.int32)
+    sm = 1.0 / np.sqrt(D)
+    got, ref, flags, _, _ = _verify(olib, w, sm)
+    assert flags == 0
+    assert_close(got, ref, "short chunks %s G=%d D=%d W=%d C=%d" % (dtype, G, D, window, C))
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "i8-bf16"])
 def test_rollback_then_decode(dtype, olib):
     """Verify 8 drafts, accept a random prefix of them, then decode the bonus
