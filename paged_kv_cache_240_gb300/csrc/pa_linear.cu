@@ -63,9 +63,12 @@ __device__ __forceinline__ float ld_act(const XT* p) {
 }
 
 // NT token groups of 8 (1 or 2).  Grid: x = channel group, y = 16-token group,
-// z = split of the k blocks.
+// z = split of the k blocks.  The loads are only in flight while their warps
+// are resident, so for up to 8 tokens the registers are held to five CTAs per
+// SM (40 warps; no spill): a 688-CTA grid, the 11008-channel projections, then
+// runs in one wave instead of a full wave and a short second one.
 template <typename XT, int NT>
-__global__ void __launch_bounds__(kThreads) int8_linear_kernel(const LinParams p) {
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 5 : 4) int8_linear_kernel(const LinParams p) {
   __shared__ float red[kWarps][NT * 8][kCh];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
