@@ -31,6 +31,13 @@
 // wait only tells a barrier's current phase from the one before, so every
 // barrier is waited on at every phase, in order (or provably within one phase);
 // every wait is bounded.
+//
+// Key split (a second instance, for chunks of at most 128 rows, such as a
+// speculative-decode verification of a few drafts): both query slots hold the
+// same rows and take the item's key tiles alternately, so two S -> softmax ->
+// P V chains run at once; the query tile the item does not need becomes a third
+// V stage; at the item's end slot 1 divides its O by its normaliser in tensor
+// memory and hands its weight log2(l) + m to slot 0, which combines the two.
 #include <algorithm>
 #include <cstring>
 #include <type_traits>
