@@ -63,6 +63,16 @@ def recorded_traffic(workload, call="decode"):
     return tr.get("traffic_bytes_per_launch", {}).get(workload)
 
 
+def max_over_ranks(torch, values, world, device="cuda"):
+    """Each rank's timings -> their maximum over the ranks (every rank gets it):
+    the job runs as long as its slowest rank.  One process: the values as given."""
+    if world <= 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -515,12 +525,8 @@ def bench_linear(args):
                 t.copy_(y, non_blocking=True)
         s1.record(stream)
         torch.cuda.synchronize()
-    total_ms = sum(step_ms)
-    e2e_ms = s0.elapsed_time(s1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([total_ms, e2e_ms], device="cuda", dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
+    total_ms, e2e_ms = max_over_ranks(torch, [sum(step_ms), s0.elapsed_time(s1) / e2e_steps],
+                                      world)
     ms_per_step = total_ms / args.steps
     value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
     peaks, peak_kind = measured_peaks()
@@ -632,13 +638,7 @@ def main():
     build()
     import paged_kv_cache_240_gb300 as pa
     r = time_ours(args, w, torch, pa, I, rank, world)
-    total_ms = r["total_ms"]
-    if world > 1:
-        t = torch.tensor([total_ms, r["e2e_ms"]], device="cuda", dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
-    else:
-        e2e_ms = r["e2e_ms"]
+    total_ms, e2e_ms = max_over_ranks(torch, [r["total_ms"], r["e2e_ms"]], world)
     ms_per_step = total_ms / args.steps
     value = world * kv_step / (ms_per_step * 1e-3) / 1e9
     peaks, peak_kind = measured_peaks()
