@@ -17,6 +17,8 @@ What pins what:
     length 1..64; closed forms (L=1, equal keys, q=0, W=1, W>=L); bit-identical
     results under a random relabelling of physical blocks; the online-softmax /
     split-K form against the two-pass definition.
+  * INT8 linear: numpy's fp64 product of the dequantised weights (plus bias);
+    weight rows quantised exactly as the KV cache write quantises a row.
 """
 import os
 
@@ -405,7 +407,40 @@ def check_bad_block_ids_left_out(lib):
         np.testing.assert_allclose(got[b:b + 1], ref, rtol=0, atol=ATOL)
 
 
-ALL_CHECKS = [
+# ------------------------------------------------------------------ INT8 linear
+
+def check_linear_dense(lib):
+    """Weight-only INT8 linear = numpy's fp64 product of the dequantised weights
+    (code * scale) with the activations, plus the bias; non-square shapes, both
+    activation types."""
+    for dtype in ("f16", "bf16"):
+        for m, n, k in ((3, 5, 7), (2, 16, 64)):
+            w = I.normal_bits((n, k), dtype, 21, m * n + k)
+            x = I.normal_bits((m, k), dtype, 22, m * n + k)
+            bias = I.normal_bits((n,), dtype, 23, m * n + k)
+            codes, scales = oracle.quantize_weights(w, dtype, lib=lib)
+            deq = codes.astype(np.float64) * scales.astype(np.float64)[:, None]
+            ref = bits_to_f64(x, dtype) @ deq.T + bits_to_f64(bias, dtype)[None, :]
+            y = oracle.linear_int8(codes, scales, x, dtype, bias_bits=bias, lib=lib)
+            np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def check_linear_weight_rows_as_kv_rows(lib):
+    """Each weight row (output channel) is quantised by the INT8 KV rule: the
+    codes and scale equal what the cache write stores for the same row."""
+    for dtype in ("f16", "bf16"):
+        n, k = 6, 64
+        w = I.normal_bits((n, k), dtype, 24, n)
+        codes, scales = oracle.quantize_weights(w, dtype, lib=lib)
+        cache = oracle.Cache("i8", 1, 1, k)
+        rows = w.reshape(n, 1, k)
+        oracle.write_kv(cache, rows, rows, dtype, np.arange(n, dtype=np.int32), lib=lib)
+        assert (cache.k_scale[0, 0, :n] == scales).all(), (cache.k_scale[0, 0, :n], scales)
+        assert (cache.k[0, 0, :n] == codes).all()
+
+
+ALL_CHECKS = [  # cheap checks first: a mutant stops at the first failure
+    check_linear_dense, check_linear_weight_rows_as_kv_rows,
     check_f16_decode, check_bf16_decode, check_decode_golden,
     check_quant_golden, check_quant_golden_through_write, check_quant_properties,
     check_write_placement,

@@ -32,6 +32,16 @@ MUTANTS = [
     ("clamp_126", "if (r > 127.0f)\n            r = 127.0f;", "if (r > 126.0f)\n            r = 126.0f;"),
     ("write_k_into_v", "void *cache = which ? v_cache : k_cache;", "void *cache = which ? k_cache : k_cache;"),
     ("dequant_no_scale", "out[d] = (double)codes[d] * scale;", "out[d] = (double)codes[d];"),
+    ("linear_no_scale", "s += xv * ((double)codes[(size_t)i * k + j] * (double)scales[i]);",
+     "s += xv * (double)codes[(size_t)i * k + j];"),
+    ("linear_scale_of_next_channel", "s += xv * ((double)codes[(size_t)i * k + j] * (double)scales[i]);",
+     "s += xv * ((double)codes[(size_t)i * k + j] * (double)scales[(i + 1) % n]);"),
+    ("linear_bias_dropped", "            if (has_bias)\n                s +=", "            if (0)\n                s +="),
+    ("linear_x_type_swapped",
+     "double xv = x_dtype == PAO_BF16 ? pao_bf16_to_double(xb) : pao_f16_to_double(xb);",
+     "double xv = x_dtype == PAO_BF16 ? pao_f16_to_double(xb) : pao_bf16_to_double(xb);"),
+    ("weights_scale_slot_shift", "pao_quantize_row(row, k, codes + (size_t)i * k, scales + i);",
+     "pao_quantize_row(row, k, codes + (size_t)i * k, scales + (i + 1) % n);"),
 ]
 
 
