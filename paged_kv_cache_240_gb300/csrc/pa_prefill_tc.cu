@@ -87,7 +87,11 @@ struct Layout {
   static constexpr int kTmemSlotOff = kFlagOff + kFlagRing * 4;
   static constexpr int kOrderOff = kTmemSlotOff + 16;  // work order [kMaxPlan] uint16
   static constexpr int kXchOff = kOrderOff + kMaxPlan * 2;  // key split: slot 1's weight per row
-  static constexpr int kUsed = kXchOff + kRows * 4;
+  // greedy work assignment: this CTA's work-list positions, their count, a done
+  // flag, and the cost totals it is decided on
+  static constexpr int kSchedOff = kXchOff + kRows * 4;
+  static constexpr int kSchedItems = 128;
+  static constexpr int kUsed = kSchedOff + kSchedItems * 2 + 6 * 4;
   // key split: both slots read query tile 0, and tile 1's space is a third V
   // stage (a V tile is exactly a Q tile: 128 rows of D 16-bit values)
   static constexpr int kV2Off = kQOff + kQBytes;
@@ -356,20 +360,50 @@ __device__ __forceinline__ Item item_info(const AttnParams& p, int n, int kvh, i
 
 // The work list: items ordered by cost (key tiles + a fixed overhead), longest
 // first, when the CTA could rank the (sequence, tile) pairs (every kv head of a
-// pair costs the same); in (sequence, kv head, tile) order otherwise.  Round r
-// of the list goes to the CTAs in alternating directions (CTA b takes position
-// r*grid + b in even rounds, r*grid + grid-1-b in odd ones), so a CTA that drew
-// a long item early draws a short one next.  Returns false past the end.
+// pair costs the same); in (sequence, kv head, tile) order otherwise.  With the
+// ranked list of a short-chunk (key-split) launch the CTAs take the items
+// greedily, each next item to the CTA with
+// the least work so far (ties to the lower index; warp 2 of every CTA computes
+// the same assignment and publishes its own CTA's part, see the kernel), when a
+// bound guarantees that no CTA gets more than kSchedItems items; otherwise
+// round r of the list goes to the CTAs in alternating directions (CTA b takes
+// position r*grid + b in even rounds, r*grid + grid-1-b in odd ones).  Either
+// way CTA b's first item is position b.  Returns false past the end (or when a
+// bounded wait for the assignment ran out).
 struct WorkList {
-  const uint16_t* order;  // pair index by rank, or nullptr
+  const uint16_t* order;  // rank -> pair index (low 9 bits) and cost (high 7), or nullptr
   int num_pairs, kv_heads, q_tiles;
+  bool greedy;
+  int first_items;                 // positions of cost > 0 (ranked list)
+  const volatile uint16_t* items;  // greedy: this CTA's positions
+  const volatile int* count;       // greedy: how many are published
+  const volatile int* done;        // greedy: all are published
 
   __device__ __forceinline__ bool at(int j, int& n, int& kvh, int& tile) const {
     const int grid = gridDim.x, b = blockIdx.x;
-    const long long s = (long long)j * grid + ((j & 1) ? grid - 1 - b : b);
+    long long s;
+    if (greedy) {
+      if (j == 0) {
+        if (b >= first_items) return false;
+        s = b;
+      } else {
+        const long long t0 = clock64();
+        while (*count <= j) {
+          if (*done) {
+            if (*count <= j) return false;
+            break;
+          }
+          if (clock64() - t0 > kWaitLimitCycles) return false;
+        }
+        __threadfence_block();
+        s = items[j];
+      }
+    } else {
+      s = (long long)j * grid + ((j & 1) ? grid - 1 - b : b);
+    }
     if (s >= (long long)num_pairs * kv_heads) return false;
     if (order) {
-      const int pair = order[s / kv_heads];
+      const int pair = order[s / kv_heads] & 0x1FF;
       kvh = (int)(s % kv_heads);
       n = pair / q_tiles;
       tile = pair % q_tiles;
@@ -417,6 +451,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* merge_ready = pv_done + kQTiles;  // KS: slot 1's (m, l) are in shared memory
   uint64_t* merge_done = merge_ready + 1;     // KS: slot 0 has read slot 1's O
   float* xch = reinterpret_cast<float*>(smem + LY::kXchOff);
+  uint16_t* sched_items = reinterpret_cast<uint16_t*>(smem + LY::kSchedOff);
+  int* sched = reinterpret_cast<int*>(smem + LY::kSchedOff + LY::kSchedItems * 2);
+  // sched[0] count, [1] done, [2] total cost, [3] largest, [4] smallest nonzero,
+  // [5] pairs of nonzero cost
   constexpr int VS = KS ? kVSMax : kVS;  // V stages in use
   uint32_t* bmask = reinterpret_cast<uint32_t*>(smem + LY::kFlagOff);  // loaded blocks per tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::kTmemSlotOff);
@@ -442,6 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(merge_ready, kSoftmaxThreads);
     mbar_init(merge_done, kSoftmaxThreads);
+    sched[0] = sched[1] = sched[2] = sched[3] = sched[5] = 0;
+    sched[4] = 0x7fffffff;
     fence_mbar_init();
   }
   if (warp == 1) {  // tensor memory: per query tile, S (P in its first half) and O
@@ -456,12 +496,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   wl.kv_heads = p.num_kv_heads;
   wl.q_tiles = p.q_tiles;
   wl.order = nullptr;
+  wl.greedy = false;
+  wl.first_items = 0;
+  wl.items = sched_items;
+  wl.count = sched;
+  wl.done = sched + 1;
+  __syncthreads();  // the scheduler's counters are set
   if (wl.num_pairs <= kMaxPlan) {
     int* cost = reinterpret_cast<int*>(smem + LY::kVOff);
     uint16_t* order = reinterpret_cast<uint16_t*>(smem + LY::kOrderOff);
     for (int j = threadIdx.x; j < wl.num_pairs; j += kThreads) {
       const Item it = item_info(p, j / p.q_tiles, 0, j % p.q_tiles, false);
-      cost[j] = it.valid ? it.ntiles + kItemCost : 0;
+      const int c = it.valid ? min(it.ntiles + kItemCost, 127) : 0;
+      cost[j] = c;
+      if (c > 0) {
+        atomicAdd(&sched[2], c * p.num_kv_heads);
+        atomicMax(&sched[3], c);
+        atomicMin(&sched[4], c);
+        atomicAdd(&sched[5], 1);
+      }
     }
     __syncthreads();
     for (int j = threadIdx.x; j < wl.num_pairs; j += kThreads) {
@@ -471,13 +524,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ci = cost[i2];
         rank += (ci > cj || (ci == cj && i2 < j)) ? 1 : 0;
       }
-      order[rank] = (uint16_t)j;
+      order[rank] = (uint16_t)(j | (cj << 9));
     }
     wl.order = order;
   }
   fence_before();
   __syncthreads();
   fence_after();
+  if (KS && wl.order && sched[5] > 0 && gridDim.x <= 160) {
+    // greedy (short chunks: many items of very different lengths; the long
+    // chunks' few large items keep the alternating order, which measured
+    // better there) when it provably fits: a CTA's work stays below
+    // total/grid + the largest cost, so it holds at most that over the smallest
+    // cost items
+    const long long bound =
+        ((long long)sched[2] / gridDim.x + sched[3] + sched[4] - 1) / sched[4] + 1;
+    wl.greedy = bound <= LY::kSchedItems;
+    wl.first_items = sched[5] * p.num_kv_heads;
+  }
   const uint32_t tmem = *tmem_slot;
   bool timed_out = false;
 
@@ -594,6 +658,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (k > 0) mbar_wait(q_full, (k - 1) & 1);
       }
       if (timed_out && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
+    } else if (warp == 2) {
+      // ---------------- scheduler: the greedy assignment, every CTA alike (lane
+      // l keeps the work of CTAs l, l+32, ..., l+128 as keys work << 8 | CTA)
+      if (wl.greedy) {
+        uint32_t load[5] = {0u, 0u, 0u, 0u, 0u};
+        int mine = 0;
+        const int grid = gridDim.x;
+        for (int s = 0; s < wl.first_items; s++) {
+          const uint32_t c = wl.order[s / wl.kv_heads] >> 9;
+          uint32_t best = 0xffffffffu;
+#pragma unroll
+          for (int q = 0; q < 5; q++)
+            if (lane + 32 * q < grid) best = min(best, (load[q] << 8) | (uint32_t)(lane + 32 * q));
+          best = __reduce_min_sync(0xffffffffu, best);
+          const int win = (int)(best & 0xffu);
+#pragma unroll
+          for (int q = 0; q < 5; q++)
+            if (win == lane + 32 * q) load[q] += c;
+          if (win == (int)blockIdx.x) {
+            if (lane == 0 && mine < LY::kSchedItems) {  // the bound keeps it below
+              sched_items[mine] = (uint16_t)s;
+              __threadfence_block();
+              *reinterpret_cast<volatile int*>(&sched[0]) = mine + 1;
+            }
+            mine++;
+          }
+        }
+        if (lane == 0) {
+          __threadfence_block();
+          *reinterpret_cast<volatile int*>(&sched[1]) = 1;
+        }
+      }
     } else if (warp == 1) {
       // ---------------- MMA warp (one elected lane issues)
       const uint32_t idS = idesc<BF>(kRows, kKeys, false);
