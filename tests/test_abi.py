@@ -100,3 +100,32 @@ def test_prefill_rejects_bad_arguments(lib):
     assert call(_cache(), mq=-1) == pa.PA_ERR_INVALID_ARG
     assert call(_cache(), qdt=2) == pa.PA_ERR_UNSUPPORTED
     assert call(_cache(), T=0) == pa.PA_OK
+
+
+def test_linear_rejects_bad_arguments():
+    """include/pa_linear.h: the host checks return before any launch (fake,
+    never dereferenced addresses; 16-byte aligned unless the case says not)."""
+    from paged_kv_cache_240_gb300 import linear as L
+    lib = L._lib()
+    A = 1 << 20  # an aligned fake address
+
+    def lin(codes=A, scales=A, x=A, y=A, xdt=pa.PA_BF16, m=8, n=64, k=256, ws=None):
+        return lib.pa_linear_int8(codes, scales, None, x, xdt, m, n, k, y, ws, 0, None)
+
+    assert lin(codes=None) == pa.PA_ERR_INVALID_ARG
+    assert lin(x=None) == pa.PA_ERR_INVALID_ARG
+    assert lin(m=0) == pa.PA_ERR_INVALID_ARG
+    assert lin(xdt=pa.PA_I8) == pa.PA_ERR_UNSUPPORTED
+    assert lin(n=24) == pa.PA_ERR_UNSUPPORTED          # n % 16
+    assert lin(k=96) == pa.PA_ERR_UNSUPPORTED          # k % 64
+    assert lin(k=65536 + 64) == pa.PA_ERR_UNSUPPORTED  # k too large
+    assert lin(codes=A + 8) == pa.PA_ERR_INVALID_ARG   # codes not 16-byte aligned
+    assert lin(x=A + 4) == pa.PA_ERR_INVALID_ARG       # x not 16-byte aligned
+    assert lin(y=A + 1) == pa.PA_ERR_INVALID_ARG       # y not 2-byte aligned
+    assert lin(scales=A + 2) == pa.PA_ERR_INVALID_ARG  # scales not 4-byte aligned
+
+    q = lib.pa_linear_int8_quantize
+    assert q(None, pa.PA_BF16, 16, 64, A, A, None) == pa.PA_ERR_INVALID_ARG
+    assert q(A, pa.PA_I8, 16, 64, A, A, None) == pa.PA_ERR_UNSUPPORTED
+    assert q(A, pa.PA_F16, 0, 64, A, A, None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_linear_int8_workspace_bytes(0, 64, 64) == 0
