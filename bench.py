@@ -130,11 +130,11 @@ class ClockSampler:
 # ------------------------------------------------------------------ device workload
 
 class DeviceStep:
-    """Everything one step needs, resident on the device."""
+    """Everything one step needs, resident on the device ``dev`` (the host serves only
+    checks of this bookkeeping that stand host functions in for the library's calls)."""
 
-    def __init__(self, w, torch, pa, I, seed):
+    def __init__(self, w, torch, pa, I, seed, dev="cuda"):
         self.w, self.torch, self.pa = w, torch, pa
-        dev = "cuda"
         src = I.source_dtype(w)
         self.cache = pa.PagedCache(w.num_blocks, w.num_kv_heads, w.head_dim, w.cache_dtype)
         self.err = torch.zeros(4, dtype=torch.int32, device=dev)
@@ -149,17 +149,18 @@ class DeviceStep:
         for i in range(0, hist.size, chunk):
             s = torch.from_numpy(hist[i:i + chunk]).to(dev)
             shape = (s.shape[0], w.num_kv_heads, w.head_dim)
-            k = I.device_normal(shape, src, seed, 2 * i + 1)
-            v = I.device_normal(shape, src, seed, 2 * i + 2)
+            k = I.device_normal(shape, src, seed, 2 * i + 1, dev)
+            v = I.device_normal(shape, src, seed, 2 * i + 2, dev)
             pa.pa_write_kv(self.cache, k, v, s, self.err)
         T = w.num_q_tokens
-        self.k_new = I.device_normal((T, w.num_kv_heads, w.head_dim), src, seed, 10 ** 7)
-        self.v_new = I.device_normal((T, w.num_kv_heads, w.head_dim), src, seed, 10 ** 7 + 1)
+        self.k_new = I.device_normal((T, w.num_kv_heads, w.head_dim), src, seed, 10 ** 7, dev)
+        self.v_new = I.device_normal((T, w.num_kv_heads, w.head_dim), src, seed, 10 ** 7 + 1,
+                                     dev)
         self.slots = torch.from_numpy(new).to(dev)
         nd = w.num_decode
         self.nd = nd
         nq = int(w.cu_q_lens[nd])
-        q = I.device_normal((T, w.num_q_heads, w.head_dim), w.q_dtype, seed, 10 ** 7 + 2)
+        q = I.device_normal((T, w.num_q_heads, w.head_dim), w.q_dtype, seed, 10 ** 7 + 2, dev)
         # decode and prefill parts as separate (aligned, contiguous) tensors
         self.q_dec, self.q_pre = q[:nq].clone(), q[nq:].clone()
         self.out_dec, self.out_pre = torch.empty_like(self.q_dec), torch.empty_like(self.q_pre)
@@ -174,7 +175,8 @@ class DeviceStep:
                                               w.max_blocks_per_seq, w.window)
         self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
         self.reduce_launched = nbytes > 0 and nd > 0
-        torch.cuda.synchronize()
+        if torch.device(dev).type == "cuda":
+            torch.cuda.synchronize()
         if int(self.err[0]) != 0:
             raise RuntimeError("device flags %d while filling the cache" % int(self.err[0]))
 
@@ -431,6 +433,21 @@ class OracleLinearSample:
         return self.bytes, time.perf_counter() - t0
 
 
+def linear_layers(torch, shapes, m, seed, dev="cuda"):
+    """(codes, scales, x, y) of each projection in ``shapes``, drawn in order from
+    one seeded generator on ``dev``: codes uniform in [-127, 127], scales uniform
+    in [0.001, 0.011], m activation rows ~N(0, 1) in bf16, y the bf16 output."""
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    mats = []
+    for n, k in shapes:
+        codes = torch.randint(-127, 128, (n, k), dtype=torch.int8, device=dev, generator=gen)
+        scales = torch.rand(n, device=dev, generator=gen) * 0.01 + 0.001
+        x = torch.randn((m, k), device=dev, generator=gen).to(torch.bfloat16)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        mats.append((codes, scales, x, y))
+    return mats
+
+
 def bench_linear(args):
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -472,14 +489,7 @@ def bench_linear(args):
     from __graft_entry__ import build
     build()
     from paged_kv_cache_240_gb300 import linear as L
-    gen = torch.Generator(device="cuda").manual_seed(args.seed + 1000 * rank)
-    mats = []
-    for n, k in shapes:
-        codes = torch.randint(-127, 128, (n, k), dtype=torch.int8, device="cuda", generator=gen)
-        scales = torch.rand(n, device="cuda", generator=gen) * 0.01 + 0.001
-        x = torch.randn((m, k), device="cuda", generator=gen).to(torch.bfloat16)
-        y = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
-        mats.append((codes, scales, x, y))
+    mats = linear_layers(torch, shapes, m, args.seed + 1000 * rank)
     nbytes = max(L.int8_workspace_bytes(m, n, k) for n, k in shapes)
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
     launches = sum(1 + (1 if L.int8_workspace_bytes(m, n, k) else 0) for n, k in shapes)

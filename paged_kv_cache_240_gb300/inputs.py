@@ -156,6 +156,9 @@ def make_workload(name: str, seed: int = 0, num_seqs: int | None = None,
     rng = np.random.default_rng([seed, 1])
     B = num_seqs if num_seqs is not None else r["num_seqs"]
     L = _lengths(lens if lens is not None else r["lens"], B, rng)[:B]
+    if L.shape[0] != B:
+        raise ValueError("%s: %d decoding sequences but %d lengths given"
+                         % (name, B, L.shape[0]))
     q_lens = np.ones(B, np.int64)
     if "num_chunks" in r:
         nc = num_chunks if num_chunks is not None else r["num_chunks"]

@@ -5,8 +5,9 @@ buffers and may not allocate device memory (a plugin inside an engine that owns
 every allocation, or a serving loop that must not call cudaMalloc/cudaFree
 because they can synchronise the device).  Its split-K partials live in scratch
 compiled into the library instead of a caller-provided workspace.  This file is
-collected last so that a run stopping at the first failure has already run every
-other test; it also passes on its own in a fresh process.
+collected after the other kernel tests (only the full-size sampled checks, which
+build whole benchmark pools, come later) so that a run stopping at the first
+failure has already run them; it also passes on its own in a fresh process.
 """
 import numpy as np
 import pytest
