@@ -344,13 +344,13 @@ class OracleSample:
     the write of the sequence's new tokens + fp64 attention of its queries, on
     the first ``heads`` kv heads (and their GQA query heads)."""
 
-    def __init__(self, w, I, nseq):
+    def __init__(self, w, I, nseq, first=0):
         import oracle
         self.oracle, self.lib, self.w = oracle, oracle.load(), w
         self.per_tok = 2 * w.head_dim * (1 if w.cache_dtype == "i8" else 2) + (
             8 if w.cache_dtype == "i8" else 0)
         self.seqs = []
-        for b in range(min(nseq, w.num_seqs)):
+        for b in range(first, min(first + nseq, w.num_seqs)):
             L, C = int(w.context_lens[b]), int(w.q_lens[b])
             nblk = -(-L // w.block_size)
             c = oracle.Cache(w.cache_dtype, nblk, w.num_kv_heads, w.head_dim)
@@ -395,6 +395,65 @@ def cpu_baseline(w, I, budget_s, nseq=8):
         b, dt = smp.run(runs)
         nbytes, spent, runs = nbytes + b, spent + dt, runs + 1
     return nbytes / spent, len(smp.seqs), runs, spent
+
+
+def _oracle_core_worker(name, seed, num_seqs, b, budget_s, barrier, results):
+    """One process of the all-cores baseline: sequence ``b``'s sample, timed for
+    ``budget_s`` seconds after every process has built its own."""
+    try:
+        from paged_kv_cache_240_gb300 import inputs as I
+        w = I.make_workload(name, seed=seed, num_seqs=num_seqs)
+        smp = OracleSample(w, I, 1, first=b % w.num_seqs)
+        smp.run(0)                                        # untimed: first touch
+        barrier.wait(timeout=300)
+        nbytes, t0 = 0, time.time()
+        while time.time() - t0 < budget_s:
+            nbytes += smp.run(0)[0]
+        results.put((b, nbytes, t0, time.time(), None))
+    except Exception as e:  # reported by the parent, which then leaves the field out
+        results.put((b, 0, 0.0, 0.0, repr(e)))
+
+
+def cpu_baseline_all_cores(w, budget_s, seed=0, num_seqs=None, procs=None):
+    """The same oracle, one process per host core (spawned, so that no process
+    forks after the GPU is in use), each on its own sequence: bytes of all of
+    them / the wall-clock window from the first start to the last end.
+    Returns (GB/s, processes) or raises."""
+    import multiprocessing as mp
+    import queue as q
+    n = procs or (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                  else os.cpu_count() or 1)
+    ctx = mp.get_context("spawn")
+    barrier, results = ctx.Barrier(n), ctx.Queue()
+    ps = [ctx.Process(target=_oracle_core_worker,
+                      args=(w.name, seed, num_seqs, b, budget_s, barrier, results), daemon=True)
+          for b in range(n)]
+    for p in ps:
+        p.start()
+    got, deadline = [], time.time() + budget_s + 300
+    try:
+        while len(got) < n:
+            try:
+                got.append(results.get(timeout=1.0))
+                if got[-1][4]:                    # failed: release the others too
+                    barrier.abort()
+                    raise RuntimeError(got[-1][4])
+                continue
+            except q.Empty:
+                pass
+            # a process that failed before reporting exits non-zero; the others
+            # would wait for it at the barrier
+            if any(p.exitcode not in (None, 0) for p in ps) or time.time() > deadline:
+                barrier.abort()
+                raise RuntimeError("%d of %d oracle processes reported" % (len(got), n))
+    finally:
+        for p in ps:
+            p.join(timeout=30)
+            if p.is_alive():
+                p.terminate()
+    nbytes = sum(g[1] for g in got)
+    window = max(g[3] for g in got) - min(g[2] for g in got)
+    return nbytes / window / 1e9, n
 
 
 # ------------------------------------------------------------------ INT8 linear
@@ -700,6 +759,15 @@ def main():
             "sample": "%d runs over the first %d of %d sequences (whole contexts, all heads): "
                       "write of each one's new tokens + fp64 attention of its queries, "
                       "%.1f s of CPU time" % (runs, nseq, w.num_seqs, spent)}
+        try:
+            va, procs = cpu_baseline_all_cores(w, args.cpu_budget, args.seed, args.num_seqs)
+            line["cpu_baseline"]["all_cores"] = {
+                "value": va, "unit": "GB/s", "cores": procs,
+                "sample": "%d concurrent processes, process i on sequence i (whole context, "
+                          "all heads), %.0f s each; bytes of all / wall-clock window"
+                          % (procs, args.cpu_budget)}
+        except Exception as e:  # the single-thread figure above stands alone
+            line["cpu_baseline"]["all_cores"] = {"unavailable": str(e)[:200]}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -1,6 +1,7 @@
 """The multi-process side of bench.py without a GPU: two ranks on the gloo
 backend (127.0.0.1) agree on the slowest rank's time, and under two ranks the
-reference arm prints exactly one line, from rank 0."""
+reference arm prints exactly one line, from rank 0; the all-cores oracle
+baseline's spawned processes report or fail fast."""
 import json
 import os
 import socket
@@ -65,3 +66,19 @@ def test_reference_arm_prints_once_under_two_ranks(workload):
     assert len(outs[0]) == 1
     line = json.loads(outs[0][0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+
+
+def test_all_cores_oracle_baseline():
+    """The all-cores CPU baseline: every spawned process reports, and one that
+    fails (here: a workload its process cannot build) ends the measurement at
+    once with that process's error instead of leaving the others waiting."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    from paged_kv_cache_240_gb300 import inputs as I
+    oracle.build()
+    w = I.make_workload("tiny", seed=0)
+    value, procs = bench.cpu_baseline_all_cores(w, 0.5, procs=2)
+    assert procs == 2 and value > 0
+    with pytest.raises(RuntimeError, match="decoding sequences"):
+        bench.cpu_baseline_all_cores(w, 0.5, num_seqs=7, procs=2)
