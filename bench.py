@@ -36,6 +36,9 @@ sys.path.insert(0, ROOT)
 METRIC = "paged-attn decode KV-read GB/s (% of GB300 HBM peak); decode steps/sec"
 DEFAULT_WORKLOAD = "mha-7b"
 L2_BYTES = 129 * 2 ** 20
+# GB300 datasheet figures, reported beside the measured peaks for context only:
+# HBM3e 7.9 TB/s, dense bf16 tensor 2.25 PFLOP/s
+NOMINAL = {"GB/s": 7900.0, "TFLOP/s": 2250.0}
 TRAFFIC_FILES = {"decode": os.path.join(ROOT, "profiles", "decode_traffic.json"),
                  "prefill": os.path.join(ROOT, "profiles", "prefill_traffic.json"),
                  "linear": os.path.join(ROOT, "profiles", "linear_traffic.json")}
@@ -613,7 +616,8 @@ def bench_linear(args):
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                          "traffic": recorded_traffic("int8-linear", "linear"),
                          "kernel": "pa_linear_int8 (int8 codes -> exact f16, mma.sync m16n8k16)",
-                         "peak_source": src + " hbm_gbs"},
+                         "peak_source": src + " hbm_gbs",
+                         "frac_of_nominal": achieved / NOMINAL["GB/s"]},
             "p10_p50_p90_step_ms": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         smp = OracleLinearSample(m, I)
@@ -738,6 +742,7 @@ def main():
                 "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name),
                 "kernel": "pa_decode (attention + split-K reduce)",
                 "peak_source": src + " hbm_gbs"}
+    roof["frac_of_nominal"] = roof["achieved"] / NOMINAL[roof["unit"]]
     cfg["launch"] = "python calls" if args.no_graph else "CUDA graph replay of the step"
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
