@@ -1,0 +1,67 @@
+"""The benchmark's algorithmic byte and flop counts (the numerators of its
+roofline figures) against brute force on small workloads: every (query, key)
+pair a query can see under the causal and window rules is enumerated, and the
+K/V rows a call must read are the distinct keys any of its queries sees, once
+per kv head."""
+import numpy as np
+import pytest
+
+import bench
+from paged_kv_cache_240_gb300 import inputs as I
+
+
+def _visible(w, b):
+    """(query position, key position) pairs of sequence b: a query at i sees j
+    with i - W < j <= i (every j <= i without a window)."""
+    L, C = int(w.context_lens[b]), int(w.q_lens[b])
+    for i in range(L - C, L):
+        for j in range(i + 1):
+            if w.window == 0 or j > i - w.window:
+                yield i, j
+
+
+def _per_token_bytes(w):
+    el = 1 if w.cache_dtype == "i8" else 2
+    scales = 2 * 4 if w.cache_dtype == "i8" else 0  # one fp32 scale each for K and V
+    return 2 * w.head_dim * el + scales
+
+
+CASES = [
+    ("mixed", dict(num_seqs=3, lens=("uniform", 1, 90), num_chunks=2, chunk_len=13, window=20)),
+    ("mixed", dict(num_seqs=2, lens=("uniform", 1, 60), num_chunks=2, chunk_len=9, window=0)),
+    ("int8-kv", dict(num_seqs=4, lens=("uniform", 1, 70))),
+    ("spec-verify", dict(num_chunks=3, chunk_len=9, window=5)),
+    ("qwen2.5-1.5b", dict(num_seqs=3, lens=("fixed", [1, 16, 33]))),
+]
+
+
+@pytest.mark.parametrize("name,kw", CASES, ids=[c[0] + "-%d" % i for i, c in enumerate(CASES)])
+def test_counts_match_brute_force(name, kw):
+    w = I.make_workload(name, seed=7, **kw)
+    per_tok = _per_token_bytes(w)
+    dec_bytes = pre_bytes = flops = 0
+    for b in range(w.num_seqs):
+        pairs = list(_visible(w, b))
+        keys = len({j for _, j in pairs})
+        if b < w.num_decode:
+            dec_bytes += keys * per_tok * w.num_kv_heads
+        else:
+            pre_bytes += keys * per_tok * w.num_kv_heads
+            flops += len(pairs) * w.num_q_heads * 4 * w.head_dim
+    assert bench.decode_kv_bytes(w) == dec_bytes
+    assert bench.prefill_kv_bytes(w) == pre_bytes
+    assert bench.prefill_flops(w) == flops
+    assert w.kv_bytes() == dec_bytes + pre_bytes
+
+
+def test_linear_bytes_by_definition():
+    """Every code byte and fp32 scale once, the 16-bit activations in and the
+    outputs out, summed over the projections."""
+    m = 5
+    shapes = [(48, 64), (16, 128)]
+    expect = 0
+    for n, k in shapes:
+        codes, scales = n * k * 1, n * 4
+        acts_in, outs = m * k * 2, m * n * 2
+        expect += codes + scales + acts_in + outs
+    assert bench.linear_bytes(m, shapes) == expect
