@@ -65,3 +65,22 @@ def test_linear_bytes_by_definition():
         acts_in, outs = m * k * 2, m * n * 2
         expect += codes + scales + acts_in + outs
     assert bench.linear_bytes(m, shapes) == expect
+
+
+def test_recorded_traffic_only_for_unchanged_sources(tmp_path, monkeypatch):
+    """The ncu traffic record is reported only while the hash of the kernel
+    sources it names matches the sources as they are; otherwise null."""
+    import json
+    rec = {"kernel_sources": ["pa_decode.cu", "pa_device.cuh"],
+           "traffic_bytes_per_launch": {"mha-7b": 123}}
+    rec["kernel_source_hash"] = bench.kernel_source_hash(rec["kernel_sources"])
+    good, stale = tmp_path / "good.json", tmp_path / "stale.json"
+    good.write_text(json.dumps(rec))
+    stale.write_text(json.dumps(dict(rec, kernel_source_hash="0" * 16)))
+    monkeypatch.setitem(bench.TRAFFIC_FILES, "decode", str(good))
+    assert bench.recorded_traffic("mha-7b") == 123
+    assert bench.recorded_traffic("int8-kv") is None
+    monkeypatch.setitem(bench.TRAFFIC_FILES, "decode", str(stale))
+    assert bench.recorded_traffic("mha-7b") is None
+    monkeypatch.setitem(bench.TRAFFIC_FILES, "decode", str(tmp_path / "missing.json"))
+    assert bench.recorded_traffic("mha-7b") is None
