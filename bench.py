@@ -76,13 +76,20 @@ def max_over_ranks(torch, values, world, device="cuda"):
     return [float(v) for v in t]
 
 
-def measured_peaks():
+def measured_peaks(path=os.path.join(ROOT, "MEASURED_PEAKS.json")):
+    """(peaks, "measured") from the measured-peaks file, or the earlier GB300
+    measurement (6.8 TB/s copy, 1.9 PFLOP/s bf16 burst, 1.7 sustained) and
+    "fallback" when the file is missing, unreadable or lacks a figure."""
+    fallback = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
     try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            return json.load(f), "measured"
-    except OSError:
-        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
-            "fallback"
+        with open(path) as f:
+            got = json.load(f)
+    except (OSError, ValueError):
+        return fallback, "fallback"
+    if not isinstance(got, dict) or not all(
+            isinstance(got.get(k), (int, float)) and got[k] > 0 for k in fallback):
+        return fallback, "fallback"
+    return got, "measured"
 
 
 # ------------------------------------------------------------------ clocks

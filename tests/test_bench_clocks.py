@@ -1,6 +1,6 @@
 """The clock record of the timed region, parsed from nvidia-smi's CSV samples
 (a stand-in process here, no GPU): median SM clock, the maximum, and every
-throttle reason seen active in any sample."""
+throttle reason seen active in any sample; and the peaks the roofline divides by."""
 import bench
 
 
@@ -43,3 +43,20 @@ def test_without_nvidia_smi():
     s = bench.ClockSampler(None)
     rec = s.stop()
     assert rec["sm_mhz"] is None and rec["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_measured_peaks_or_fallback(tmp_path):
+    import json
+    good = tmp_path / "peaks.json"
+    good.write_text(json.dumps({"hbm_gbs": 6792.1, "bf16_tflops": 1930.6,
+                                "bf16_tflops_sustained": 1716.1, "chip": "GB300"}))
+    peaks, kind = bench.measured_peaks(str(good))
+    assert kind == "measured" and peaks["hbm_gbs"] == 6792.1
+    partial = tmp_path / "partial.json"
+    partial.write_text(json.dumps({"hbm_gbs": 6792.1}))
+    for path in (partial, tmp_path / "missing.json"):
+        peaks, kind = bench.measured_peaks(str(path))
+        assert kind == "fallback" and peaks["hbm_gbs"] == 6800.0 and peaks["bf16_tflops"] == 1900.0
+    bad = tmp_path / "bad.json"
+    bad.write_text("{not json")
+    assert bench.measured_peaks(str(bad))[1] == "fallback"
