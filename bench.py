@@ -253,6 +253,40 @@ def decode_kv_bytes(w):
     return int(eff.sum()) * per_tok * w.num_kv_heads
 
 
+def roofline(w, dec_ms, pre_ms, peaks, src):
+    """The roofline object of the call that takes longer: the prefill call against
+    the bf16 tensor peak when its flop per algorithmic byte exceeds the machine
+    balance, else against HBM; otherwise the decode call against HBM.  ``achieved``
+    = the call's algorithmic flops or bytes / its mean CUDA-event time (ms)."""
+    pre_flops, pre_bytes = prefill_flops(w), prefill_kv_bytes(w)
+    balance = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)  # flop per byte
+    if pre_ms > dec_ms and pre_flops > balance * pre_bytes:
+        # the prefill kernel dominates and is a dense contraction: tensor-core roofline
+        achieved = pre_flops / (pre_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": recorded_traffic(w.name, "prefill"),
+                "kernel": ("pa_prefill_chunk (tcgen05.mma kind::f16, TMEM accumulators)"
+                           if w.cache_dtype != "i8" else "pa_prefill_chunk (mma.sync m16n8k16)"),
+                "peak_source": src + " bf16_tflops (burst)"}
+    elif pre_ms > dec_ms:
+        # the prefill kernel dominates with few queries per key (verification of a
+        # few drafted tokens): it streams the cache, HBM roofline
+        achieved = pre_bytes / (pre_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name, "prefill"),
+                "kernel": "pa_prefill_chunk (%d queries per sequence)" % int(w.q_lens.max()),
+                "peak_source": src + " hbm_gbs"}
+    else:
+        achieved = decode_kv_bytes(w) / (dec_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name),
+                "kernel": "pa_decode (attention + split-K reduce)",
+                "peak_source": src + " hbm_gbs"}
+    roof["frac_of_nominal"] = roof["achieved"] / NOMINAL[roof["unit"]]
+    return roof
+
+
 def capture(torch, fn, stream):
     """CUDA graph of fn's launches (the library's kernels enqueue on the current
     stream, so they are captured like any other work)."""
@@ -724,32 +758,7 @@ def main():
     peaks, peak_kind = measured_peaks()
     dec_ms, pre_ms = statistics.mean(r["dec_ms"]), statistics.mean(r["pre_ms"])
     src = peak_kind + " (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
-    pre_flops, pre_bytes = prefill_flops(w), prefill_kv_bytes(w)
-    balance = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)  # flop per byte
-    if pre_ms > dec_ms and pre_flops > balance * pre_bytes:
-        # the prefill kernel dominates and is a dense contraction: tensor-core roofline
-        achieved = pre_flops / (pre_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                "traffic": recorded_traffic(w.name, "prefill"),
-                "kernel": ("pa_prefill_chunk (tcgen05.mma kind::f16, TMEM accumulators)"
-                           if w.cache_dtype != "i8" else "pa_prefill_chunk (mma.sync m16n8k16)"),
-                "peak_source": src + " bf16_tflops (burst)"}
-    elif pre_ms > dec_ms:
-        # the prefill kernel dominates with few queries per key (verification of a
-        # few drafted tokens): it streams the cache, HBM roofline
-        achieved = pre_bytes / (pre_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name, "prefill"),
-                "kernel": "pa_prefill_chunk (%d queries per sequence)" % int(w.q_lens.max()),
-                "peak_source": src + " hbm_gbs"}
-    else:
-        achieved = decode_kv_bytes(w) / (dec_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name),
-                "kernel": "pa_decode (attention + split-K reduce)",
-                "peak_source": src + " hbm_gbs"}
-    roof["frac_of_nominal"] = roof["achieved"] / NOMINAL[roof["unit"]]
+    roof = roofline(w, dec_ms, pre_ms, peaks, src)
     cfg["launch"] = "python calls" if args.no_graph else "CUDA graph replay of the step"
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,

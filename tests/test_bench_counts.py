@@ -2,7 +2,7 @@
 roofline figures) against brute force on small workloads: every (query, key)
 pair a query can see under the causal and window rules is enumerated, and the
 K/V rows a call must read are the distinct keys any of its queries sees, once
-per kv head."""
+per kv head; and the roofline object built from them."""
 import numpy as np
 import pytest
 
@@ -84,3 +84,27 @@ def test_recorded_traffic_only_for_unchanged_sources(tmp_path, monkeypatch):
     assert bench.recorded_traffic("mha-7b") is None
     monkeypatch.setitem(bench.TRAFFIC_FILES, "decode", str(tmp_path / "missing.json"))
     assert bench.recorded_traffic("mha-7b") is None
+
+
+PEAKS = {"hbm_gbs": 6792.1, "bf16_tflops": 1930.6, "bf16_tflops_sustained": 1716.1}
+
+
+def test_roofline_picks_the_longer_call_and_its_bound():
+    """mixed: the prefill call is longer and far above the machine balance
+    (tensor); spec-verify: prefill longer, 54 flop per byte (HBM); mha-7b: the
+    decode call (HBM).  achieved = algorithmic count / the call's time."""
+    mixed = I.make_workload("mixed", seed=0)
+    r = bench.roofline(mixed, 0.02, 0.08, PEAKS, "measured")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - bench.prefill_flops(mixed) / 0.08e-3 / 1e12) < 1e-9
+    assert abs(r["frac"] - r["achieved"] / 1930.6) < 1e-12
+    assert abs(r["frac_of_nominal"] - r["achieved"] / 2250.0) < 1e-12
+    sv = I.make_workload("spec-verify", seed=0)
+    r = bench.roofline(sv, 0.0, 0.15, PEAKS, "measured")
+    assert r["bound"] == "hbm" and "prefill" in r["kernel"]
+    assert abs(r["achieved"] - bench.prefill_kv_bytes(sv) / 0.15e-3 / 1e9) < 1e-9
+    mha = I.make_workload("mha-7b", seed=0)
+    r = bench.roofline(mha, 0.37, 0.0, PEAKS, "measured")
+    assert r["bound"] == "hbm" and "decode" in r["kernel"]
+    assert abs(r["achieved"] - bench.decode_kv_bytes(mha) / 0.37e-3 / 1e9) < 1e-9
+    assert abs(r["frac_of_nominal"] - r["achieved"] / 7900.0) < 1e-12
