@@ -42,6 +42,13 @@ MUTANTS = [
      "double xv = x_dtype == PAO_BF16 ? pao_f16_to_double(xb) : pao_bf16_to_double(xb);"),
     ("weights_scale_slot_shift", "pao_quantize_row(row, k, codes + (size_t)i * k, scales + i);",
      "pao_quantize_row(row, k, codes + (size_t)i * k, scales + (i + 1) % n);"),
+    ("causal_mask_off", "*hi = i < L - 1 ? i : L - 1;", "*hi = L - 1;"),
+    ("window_of_one_ignored", "*lo = (window > 0 && i - window + 1 > 0)",
+     "*lo = (window > 1 && i - window + 1 > 0)"),
+    ("v_dequantised_with_k_scale", "(double)(which ? c->v_scale : c->k_scale)[r]",
+     "(double)(which ? c->k_scale : c->k_scale)[r]"),
+    ("v_scale_stored_in_k_scales", "float *sc = which ? v_scale : k_scale;",
+     "float *sc = which ? k_scale : k_scale;"),
 ]
 
 
