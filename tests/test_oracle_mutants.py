@@ -49,6 +49,10 @@ MUTANTS = [
      "(double)(which ? c->k_scale : c->k_scale)[r]"),
     ("v_scale_stored_in_k_scales", "float *sc = which ? v_scale : k_scale;",
      "float *sc = which ? k_scale : k_scale;"),
+    ("online_acc_not_rescaled", "op[d] *= corr;", "op[d] *= 1.0;"),
+    ("segment_last_key_dropped", "for (int j = j0; j <= j1; j++) {\n                            long r",
+     "for (int j = j0; j < j1; j++) {\n                            long r"),
+    ("merge_o_unweighted", "o[d] += w * po[(size_t)p * D + d];", "o[d] += po[(size_t)p * D + d];"),
 ]
 
 
