@@ -53,6 +53,11 @@ MUTANTS = [
     ("segment_last_key_dropped", "for (int j = j0; j <= j1; j++) {\n                            long r",
      "for (int j = j0; j < j1; j++) {\n                            long r"),
     ("merge_o_unweighted", "o[d] += w * po[(size_t)p * D + d];", "o[d] += po[(size_t)p * D + d];"),
+    ("amax_signed", "float a = fabsf(x[d]);", "float a = x[d];"),
+    ("negative_clamp_126", "if (r < -127.0f)\n            r = -127.0f;",
+     "if (r < -126.0f)\n            r = -126.0f;"),
+    ("linear_bias_as_f16", "s += x_dtype == PAO_BF16 ? pao_bf16_to_double(bias[i])",
+     "s += x_dtype == PAO_F16 ? pao_bf16_to_double(bias[i])"),
 ]
 
 
