@@ -44,8 +44,12 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     os.makedirs(BUILD, exist_ok=True)
     srcs = sources()
 
+    # objects named for this process: several processes that build at once
+    # (ranks starting together) never link one another's half-written objects
+    tag = ".%d.o" % os.getpid()
+
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + tag)
         cmd = [NVCC, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -61,4 +65,9 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     tmp = LIB + ".tmp%d" % os.getpid()
     subprocess.check_call([NVCC, *ARCH, "-shared", "-o", tmp] + [o for o, _ in results])
     os.replace(tmp, LIB)
+    for obj, _ in results:
+        try:
+            os.remove(obj)
+        except OSError:
+            pass
     return LIB
