@@ -36,6 +36,7 @@ sys.path.insert(0, ROOT)
 METRIC = "paged-attn decode KV-read GB/s (% of GB300 HBM peak); decode steps/sec"
 DEFAULT_WORKLOAD = "mha-7b"
 L2_BYTES = 129 * 2 ** 20
+FILL_CHUNK = 1 << 15  # history rows per pa_write_kv while a pool is filled
 # GB300 datasheet figures, reported beside the measured peaks for context only:
 # HBM3e 7.9 TB/s, dense bf16 tensor 2.25 PFLOP/s
 NOMINAL = {"GB/s": 7900.0, "TFLOP/s": 2250.0}
@@ -155,7 +156,7 @@ class DeviceStep:
             L, C = int(w.context_lens[b]), int(w.q_lens[b])
             hist.append(w.slots(b, np.arange(0, L - C)))
         hist = np.concatenate(hist).astype(np.int32)
-        chunk = 1 << 15
+        chunk = FILL_CHUNK
         for i in range(0, hist.size, chunk):
             s = torch.from_numpy(hist[i:i + chunk]).to(dev)
             shape = (s.shape[0], w.num_kv_heads, w.head_dim)

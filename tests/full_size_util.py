@@ -6,10 +6,11 @@ are built by bench.DeviceStep."""
 import numpy as np
 import torch
 
+import bench
 import oracle
 from paged_kv_cache_240_gb300 import inputs as I
 
-CHUNK = 1 << 15     # history rows per pa_write_kv of the benchmark's fill
+CHUNK = bench.FILL_CHUNK  # history rows per pa_write_kv of the benchmark's fill
 SEED = 0            # the benchmark's default seed on rank 0
 EDGE_ROWS = 48      # rows checked at each end of a prefill chunk
 
