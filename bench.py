@@ -369,6 +369,9 @@ def time_ours(args, w, torch, pa, I, rank, world):
         nk = max(3, min(args.steps, 500))
         dec_ms = time_replays(torch, stream, run_dec, nk, flush)
         pre_ms = time_replays(torch, stream, run_pre, nk, flush) if st.max_q else [0.0]
+        # the same step launched call by call from Python, for comparison with the
+        # graph replays above
+        eager_ms = time_replays(torch, stream, step, nk, flush) if not args.no_graph else step_ms
         torch.cuda.synchronize()
         if int(st.err[0]) != 0:
             raise RuntimeError("device flags %d during the timed steps" % int(st.err[0]))
@@ -392,7 +395,8 @@ def time_ours(args, w, torch, pa, I, rank, world):
         s1.record(stream)
         torch.cuda.synchronize()
     e2e_ms = s0.elapsed_time(s1) / e2e_steps
-    return dict(step_ms=step_ms, dec_ms=dec_ms, pre_ms=pre_ms, total_ms=sum(step_ms),
+    return dict(step_ms=step_ms, dec_ms=dec_ms, pre_ms=pre_ms, eager_ms=eager_ms,
+                total_ms=sum(step_ms),
                 clocks=clk, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                 launches=st.launches_per_step() * args.steps, reduce=st.reduce_launched)
 
@@ -790,7 +794,8 @@ def main():
             "gpu_launches": r["launches"],
             "roofline": roof,
             "decode_call_ms": dec_ms, "prefill_call_ms": pre_ms,
-            "p10_p50_p90_step_ms": [float(np.percentile(r["step_ms"], p)) for p in (10, 50, 90)]}
+            "p10_p50_p90_step_ms": [float(np.percentile(r["step_ms"], p)) for p in (10, 50, 90)],
+            "median_step_ms_python_launches": float(np.median(r["eager_ms"]))}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, nseq, runs, spent = cpu_baseline(w, I, args.cpu_budget)
         line["cpu_baseline"] = {
