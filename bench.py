@@ -676,7 +676,9 @@ def bench_linear(args):
             "gpu_launches": launches * args.steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": recorded_traffic("int8-linear", "linear"),
+                         # the record is of the default stack (four layers, 8 tokens)
+                         "traffic": (recorded_traffic("int8-linear", "linear")
+                                     if (layers, m) == (LINEAR_LAYERS, 8) else None),
                          "kernel": "pa_linear_int8 (int8 codes -> exact f16, mma.sync m16n8k16)",
                          "peak_source": src + " hbm_gbs",
                          "frac_of_nominal": achieved / NOMINAL["GB/s"]},
