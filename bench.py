@@ -254,11 +254,12 @@ def decode_kv_bytes(w):
     return int(eff.sum()) * per_tok * w.num_kv_heads
 
 
-def roofline(w, dec_ms, pre_ms, peaks, src):
+def roofline(w, dec_ms, pre_ms, peaks, src, full_size=True):
     """The roofline object of the call that takes longer: the prefill call against
     the bf16 tensor peak when its flop per algorithmic byte exceeds the machine
     balance, else against HBM; otherwise the decode call against HBM.  ``achieved``
-    = the call's algorithmic flops or bytes / its mean CUDA-event time (ms)."""
+    = the call's algorithmic flops or bytes / its mean CUDA-event time (ms).  The
+    recorded ncu traffic is of the full-size workloads only (else null)."""
     pre_flops, pre_bytes = prefill_flops(w), prefill_kv_bytes(w)
     balance = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)  # flop per byte
     if pre_ms > dec_ms and pre_flops > balance * pre_bytes:
@@ -284,6 +285,8 @@ def roofline(w, dec_ms, pre_ms, peaks, src):
                 "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name),
                 "kernel": "pa_decode (attention + split-K reduce)",
                 "peak_source": src + " hbm_gbs"}
+    if not full_size:
+        roof["traffic"] = None
     roof["frac_of_nominal"] = roof["achieved"] / NOMINAL[roof["unit"]]
     return roof
 
@@ -782,7 +785,7 @@ def main():
     peaks, peak_kind = measured_peaks()
     dec_ms, pre_ms = statistics.mean(r["dec_ms"]), statistics.mean(r["pre_ms"])
     src = peak_kind + " (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
-    roof = roofline(w, dec_ms, pre_ms, peaks, src)
+    roof = roofline(w, dec_ms, pre_ms, peaks, src, full_size=args.num_seqs is None)
     cfg["launch"] = "python calls" if args.no_graph else "CUDA graph replay of the step"
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,

@@ -108,3 +108,9 @@ def test_roofline_picks_the_longer_call_and_its_bound():
     assert r["bound"] == "hbm" and "decode" in r["kernel"]
     assert abs(r["achieved"] - bench.decode_kv_bytes(mha) / 0.37e-3 / 1e9) < 1e-9
     assert abs(r["frac_of_nominal"] - r["achieved"] / 7900.0) < 1e-12
+
+
+def test_roofline_traffic_only_for_full_size():
+    w = I.make_workload("mha-7b", seed=0, num_seqs=16)
+    r = bench.roofline(w, 0.1, 0.0, PEAKS, "measured", full_size=False)
+    assert r["traffic"] is None and r["bound"] == "hbm"
