@@ -234,7 +234,10 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 // The f16 with bit pattern 0x64XX is 1024 + XX exactly, so a code c in
 // [-128, 127] turned into the byte c + 128 (flip the top bit) and placed under
-// 0x64 is 1024 + 128 + c; subtracting 1152 leaves c exactly.
+// 0x64 is 1024 + 128 + c; subtracting 1152 leaves c exactly.  This is the
+// published "magic number" integer-to-float conversion used by mixed-input
+// GEMMs (Kim et al., "Who Says Elephants Can't Run: Bringing Large Scale MoE
+// Models into Cloud Scale Production", 2022, Sec. 4), restated here.
 __device__ __forceinline__ uint32_t f16x2_minus_1152(uint32_t biased) {
   const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
   __half2 h = __hsub2(*reinterpret_cast<__half2*>(&biased), bias);
