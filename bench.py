@@ -326,7 +326,12 @@ def time_replays(torch, stream, run, n, flush=None):
     return [a.elapsed_time(b) for a, b in ev]
 
 
-def time_ours(args, w, torch, pa, I, rank, world):
+def time_ours(args, w, torch, pa, I, rank, world, steps=None, warmup=None):
+    """Time K graph replays of the step (after W warm-ups) on this rank, then the
+    two attention calls on their own, the step launched call by call, and the
+    step end to end through pinned host memory."""
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     st = DeviceStep(w, torch, pa, I, seed=args.seed + 1000 * rank)
     stream = torch.cuda.Stream()
@@ -357,19 +362,19 @@ def time_ours(args, w, torch, pa, I, rank, world):
         scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
         flush = scratch.zero_
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             run_step()
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         clocks.start()
         time.sleep(0.3)
-        step_ms = time_replays(torch, stream, run_step, args.steps, flush)
+        step_ms = time_replays(torch, stream, run_step, steps, flush)
         if world > 1:
             torch.distributed.barrier()
         clk = clocks.stop()
         # the two attention calls on their own, for the per-kernel roofline
-        nk = max(3, min(args.steps, 500))
+        nk = max(3, min(steps, 500))
         dec_ms = time_replays(torch, stream, run_dec, nk, flush)
         pre_ms = time_replays(torch, stream, run_pre, nk, flush) if st.max_q else [0.0]
         # the same step launched call by call from Python, for comparison with the
@@ -385,7 +390,7 @@ def time_ours(args, w, torch, pa, I, rank, world):
                                   ).pin_memory() for name in st.OUTPUTS}
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = sum(t.numel() * t.element_size() for t in outs.values())
-        e2e_steps = max(3, min(args.steps, 200))
+        e2e_steps = max(3, min(steps, 200))
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         s0.record(stream)
@@ -401,7 +406,8 @@ def time_ours(args, w, torch, pa, I, rank, world):
     return dict(step_ms=step_ms, dec_ms=dec_ms, pre_ms=pre_ms, eager_ms=eager_ms,
                 total_ms=sum(step_ms),
                 clocks=clk, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
-                launches=st.launches_per_step() * args.steps, reduce=st.reduce_launched)
+                launches=st.launches_per_step() * steps, reduce=st.reduce_launched,
+                flushed=flush is not None)
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -704,6 +710,92 @@ def bench_linear(args):
 
 # ------------------------------------------------------------------ main
 
+# The other configurations of the method's workloads, measured after the headline
+# in the default single-GPU run and reported under "workloads".
+EXTRA_WORKLOADS = ("int8-kv", "qwen2.5-1.5b", "mixed", "spec-verify")
+EXTRA_MIN_STEPS = 200  # the small steps (16 us - 0.3 ms) need more than a handful
+
+
+def workload_config(w):
+    """The ``config`` object of a paged-attention workload's line."""
+    return {"workload": w.name, "num_seqs": w.num_seqs, "num_decode": w.num_decode,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "block_size": w.block_size, "cache_dtype": w.cache_dtype,
+            "q_dtype": w.q_dtype, "window": w.window, "num_blocks": w.num_blocks,
+            "mean_context": float(w.context_lens[:w.num_decode].mean() if w.num_decode
+                                  else w.context_lens.mean()),
+            "kv_bytes_per_step": w.kv_bytes(),
+            "l2": ("L2 flushed before every timed run (a %d MB buffer written); the e2e "
+                   "loop is not flushed" % (2 * L2_BYTES >> 20)) if needs_l2_flush(w) else
+                  "inputs larger than L2 (%d MB of KV per step)" % (w.kv_bytes() >> 20)}
+
+
+def measure(args, w, torch, pa, I, rank, world, steps, warmup, peaks, src):
+    """One workload's timed steps -> the fields of its JSON line (value, timing,
+    roofline of the dominant call, clocks, end to end, launch count)."""
+    r = time_ours(args, w, torch, pa, I, rank, world, steps, warmup)
+    total_ms, e2e_ms = max_over_ranks(torch, [r["total_ms"], r["e2e_ms"]], world)
+    kv_step = w.kv_bytes()
+    ms_per_step = total_ms / steps
+    value = world * kv_step / (ms_per_step * 1e-3) / 1e9
+    dec_ms, pre_ms = statistics.mean(r["dec_ms"]), statistics.mean(r["pre_ms"])
+    roof = roofline(w, dec_ms, pre_ms, peaks, src, full_size=args.num_seqs is None)
+    cfg = workload_config(w)
+    cfg["launch"] = "python calls" if args.no_graph else "CUDA graph replay of the step"
+    fields = {"value": value, "unit": "GB/s", "steps": steps, "warmup": warmup,
+              "ms_per_step": ms_per_step, "steps_per_s": 1e3 / ms_per_step * world,
+              "hbm_frac": value / peaks["hbm_gbs"], "config": cfg, "clocks": r["clocks"],
+              "l2_flushed": r["flushed"],
+              "e2e": {"value": world * kv_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                      "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+              "gpu_launches": r["launches"], "roofline": roof,
+              "decode_call_ms": dec_ms, "prefill_call_ms": pre_ms,
+              "p10_p50_p90_step_ms": [float(np.percentile(r["step_ms"], p)) for p in (10, 50, 90)],
+              "median_step_ms_python_launches": float(np.median(r["eager_ms"]))}
+    if roof["bound"] == "tensor" and dec_ms > 0:
+        # the decode half of a mixed step, against HBM
+        achieved = decode_kv_bytes(w) / (dec_ms * 1e-3) / 1e9
+        fields["decode_roofline"] = {"bound": "hbm", "achieved": achieved,
+                                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                     "frac": achieved / peaks["hbm_gbs"],
+                                     "kernel": "pa_decode", "peak_source": src + " hbm_gbs"}
+    return fields
+
+
+def reference_line(args, w, I):
+    """The oracle (single-threaded C, fp64) timed on a bounded sample of the
+    workload per step: the line reports what was measured -- the sample's bytes
+    over the sample's time -- and says what the sample was."""
+    import oracle
+    oracle.build()
+    smp = OracleSample(w, I, nseq=4)
+    # size each step's sample so that the whole run stays near two minutes
+    per_step_s = min(args.cpu_budget, 120.0 / max(1, args.warmup + args.steps))
+    b, dt = smp.run(0)
+    heads = max(1, min(w.num_kv_heads, int(w.num_kv_heads * per_step_s / max(dt, 1e-6))))
+    nbytes, secs = 0, 0.0
+    for i in range(args.warmup + args.steps):
+        b, dt = smp.run(i, heads)
+        if i >= args.warmup:
+            nbytes, secs = nbytes + b, secs + dt
+    value = nbytes / secs / 1e9
+    sample = ("per step: one of the first %d sequences (whole context), %d of %d kv heads: "
+              "write of its new tokens + fp64 attention of its queries; %.3f MB and %.3f s per "
+              "step on average" % (len(smp.seqs), heads, w.num_kv_heads,
+                                   nbytes / args.steps / 1e6, secs / args.steps))
+    cfg = workload_config(w)
+    cfg["sample_bytes_per_step"] = nbytes / args.steps
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": cfg,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -720,6 +812,10 @@ def main():
                     help="int8-linear only: layers per step (default %d)" % LINEAR_LAYERS)
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="fewer decoding sequences (small profiling captures)")
+    ap.add_argument("--extra-workloads", default="auto",
+                    help="comma-separated workloads measured after the headline and reported "
+                         "under 'workloads'; 'auto' = %s on one GPU with the default workload, "
+                         "'none' = no others" % ",".join(EXTRA_WORKLOADS))
     args = ap.parse_args()
 
     if args.workload == "int8-linear":
@@ -729,48 +825,19 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     from paged_kv_cache_240_gb300 import inputs as I
     w = I.make_workload(args.workload, seed=args.seed, num_seqs=args.num_seqs)
-    cfg = {"workload": args.workload, "num_seqs": w.num_seqs, "num_decode": w.num_decode,
-           "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
-           "head_dim": w.head_dim, "block_size": w.block_size, "cache_dtype": w.cache_dtype,
-           "q_dtype": w.q_dtype, "window": w.window, "num_blocks": w.num_blocks,
-           "mean_context": float(w.context_lens[:w.num_decode].mean() if w.num_decode
-                                 else w.context_lens.mean()),
-           "kv_bytes_per_step": w.kv_bytes(),
-           "l2": ("L2 flushed before every timed run (a %d MB buffer written); the e2e "
-                  "loop is not flushed" % (2 * L2_BYTES >> 20)) if needs_l2_flush(w) else
-                 "inputs larger than L2 (%d MB of KV per step)" % (w.kv_bytes() >> 20)}
-    kv_step = w.kv_bytes()
 
     if args.impl == "reference":
-        if rank != 0:
-            return
-        import oracle
-        oracle.build()
-        smp = OracleSample(w, I, nseq=4)
-        # size each step's sample so that the whole run stays near two minutes
-        per_step_s = min(args.cpu_budget, 120.0 / max(1, args.warmup + args.steps))
-        b, dt = smp.run(0)
-        heads = max(1, min(w.num_kv_heads, int(w.num_kv_heads * per_step_s / max(dt, 1e-6))))
-        rates = []
-        for i in range(args.warmup + args.steps):
-            b, dt = smp.run(i, heads)
-            if i >= args.warmup:
-                rates.append(b / dt)
-        value = statistics.median(rates) / 1e9
-        sample = ("per step: one of the first %d sequences (whole context), %d of %d kv heads: "
-                  "write of its new tokens + fp64 attention of its queries" % (len(smp.seqs), heads,
-                                                                w.num_kv_heads))
-        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
-                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": kv_step / (value * 1e9) * 1e3, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": cfg,
-                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                 "sample": sample},
-                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
+        if rank == 0:
+            print(json.dumps(reference_line(args, w, I)))
         return
+
+    if args.extra_workloads == "auto":
+        extras = list(EXTRA_WORKLOADS) if (world == 1 and args.workload == DEFAULT_WORKLOAD) \
+            else []
+    elif args.extra_workloads in ("", "none"):
+        extras = []
+    else:
+        extras = [x for x in args.extra_workloads.split(",") if x and x != args.workload]
 
     import torch
     if world > 1:
@@ -778,29 +845,14 @@ def main():
     from __graft_entry__ import build
     build()
     import paged_kv_cache_240_gb300 as pa
-    r = time_ours(args, w, torch, pa, I, rank, world)
-    total_ms, e2e_ms = max_over_ranks(torch, [r["total_ms"], r["e2e_ms"]], world)
-    ms_per_step = total_ms / args.steps
-    value = world * kv_step / (ms_per_step * 1e-3) / 1e9
     peaks, peak_kind = measured_peaks()
-    dec_ms, pre_ms = statistics.mean(r["dec_ms"]), statistics.mean(r["pre_ms"])
     src = peak_kind + " (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
-    roof = roofline(w, dec_ms, pre_ms, peaks, src, full_size=args.num_seqs is None)
-    cfg["launch"] = "python calls" if args.no_graph else "CUDA graph replay of the step"
-    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+    f = measure(args, w, torch, pa, I, rank, world, args.steps, args.warmup, peaks, src)
+    line = {"metric": METRIC, "value": f["value"], "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": f["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": w.cache_dtype, "data": "synthetic", "config": cfg,
-            "steps_per_s": 1e3 / ms_per_step * world,
-            "hbm_frac": value / peaks["hbm_gbs"],
-            "clocks": r["clocks"],
-            "e2e": {"value": world * kv_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-            "gpu_launches": r["launches"],
-            "roofline": roof,
-            "decode_call_ms": dec_ms, "prefill_call_ms": pre_ms,
-            "p10_p50_p90_step_ms": [float(np.percentile(r["step_ms"], p)) for p in (10, 50, 90)],
-            "median_step_ms_python_launches": float(np.median(r["eager_ms"]))}
+            "dtype": w.cache_dtype, "data": "synthetic", "config": f["config"]}
+    line.update({k: v for k, v in f.items() if k not in line and k not in ("steps", "warmup")})
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, nseq, runs, spent = cpu_baseline(w, I, args.cpu_budget)
         line["cpu_baseline"] = {
@@ -817,6 +869,16 @@ def main():
                           % (procs, args.cpu_budget)}
         except Exception as e:  # the single-thread figure above stands alone
             line["cpu_baseline"]["all_cores"] = {"unavailable": str(e)[:200]}
+    if extras:
+        # the other configurations, one at a time, each pool freed before the next
+        line["workloads"] = {}
+        for name in extras:
+            torch.cuda.empty_cache()
+            wx = I.make_workload(name, seed=args.seed, num_seqs=args.num_seqs)
+            line["workloads"][name] = measure(
+                args, wx, torch, pa, I, rank, world, max(args.steps, EXTRA_MIN_STEPS),
+                max(args.warmup, 3), peaks, src)
+        torch.cuda.empty_cache()
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

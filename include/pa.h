@@ -40,6 +40,12 @@
  *   - Supported: block_size 16, head_dim 64 or 128, 16-bit caches (fp16, bf16)
  *     with q of the same type, int8 caches with fp16 or bf16 q.  `out` has q's
  *     type.  Every device pointer must be 16-byte aligned.
+ *   - int8 caches: any finite magnitudes.  The kernels' tensor-core operands are
+ *     f16; a bf16 query row beyond the f16 range is scaled by a power of two
+ *     into it (and its scores back), and each token's V scale enters the P V
+ *     product relative to a running reference, so rows of any scale (1e-30 or
+ *     1e30 with bf16 q and output), mixed in one sequence, keep errors relative
+ *     to the output.
  *
  * Errors
  *   - Problems visible on the host (NULL pointers, unsupported shapes or types,
@@ -173,7 +179,10 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads
  *     would exceed PA_NOALLOC_SCRATCH_BYTES (pa_decode_workspace_bytes with
  *     partition_blocks = 0 gives the size); use pa_decode for such batches.
  *   - The first call on each device looks up the scratch's device address with
- *     that device current; make that first call before any stream capture.
+ *     that device current; make that first call before any stream capture.  A
+ *     device reset (cudaDeviceReset) ends the context that address belongs to:
+ *     the next call on that device sees a new context and looks the address up
+ *     again, so after a reset, too, call once before capturing.
  *   - All calls on a device share the one scratch array and it keeps the last
  *     call's contents (nothing in it needs to start at zero).  Calls that can
  *     run at the same time on the GPU -- on different streams, or from host
@@ -219,6 +228,22 @@ const char *pa_last_cuda_error(void);
 
 /* PA_OK when flags == 0, else PA_ERR_DEVICE_DATA (flags read back by the caller). */
 pa_status pa_check_flags(int32_t flags);
+
+/*
+ * pa_selftest_bounded_wait -- checks, on the current device, the bounded wait that
+ * every in-kernel wait of this library uses (the pages have no counterpart; the
+ * library's own failure handling: a wait that runs out reports PA_FLAG_TIMEOUT
+ * and the kernel returns instead of hanging).  One small kernel waits, limited to
+ * limit_cycles SM clock cycles (1 .. 4e9), on a barrier that nothing completes,
+ * once from one thread and once as a whole warp's vote, with no copy in flight;
+ * and once on a barrier that has completed.
+ *   result    device int64[4]: [0] 1 if the one-thread wait gave up, [1] 1 if the
+ *             warp's wait gave up, [2] 1 if the completed barrier's wait returned
+ *             at once, [3] SM cycles the one-thread wait took
+ *   err_flag  receives PA_FLAG_TIMEOUT from each wait that gave up
+ */
+pa_status pa_selftest_bounded_wait(long long limit_cycles, long long *result,
+                                   int32_t *err_flag, void *stream);
 
 #ifdef __cplusplus
 }

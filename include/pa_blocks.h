@@ -43,6 +43,9 @@ typedef struct {
     long long published_blocks;  /* blocks registered under a prefix key */
     long long prefix_hit_blocks; /* blocks attached from the prefix cache (not recomputed) */
     int shared_blocks;           /* blocks currently held by more than one sequence */
+    int cached_blocks;           /* registered blocks no sequence holds, kept for reuse */
+    long long revived_blocks;    /* prefix hits on cached blocks (no holder at the time) */
+    long long reclaimed_blocks;  /* cached blocks taken back for new positions (LRU) */
 } pa_blocks_stats;
 
 /*
@@ -58,9 +61,11 @@ void pa_blocks_destroy(pa_blocks *bm);
 
 /*
  * pa_blocks_append -- reserve num_tokens new positions at the end of sequence
- * seq, taking blocks from the free list (O(1) each) as the context crosses block
- * boundaries, and write the new positions' slots to slots_out[num_tokens].
- * All or nothing: PA_ERR_OUT_OF_BLOCKS when the pool lacks free blocks,
+ * seq, taking blocks from the free list (O(1) each), and when it is empty from
+ * the prefix cache (least recently used first, O(1) each), as the context
+ * crosses block boundaries, and write the new positions' slots to
+ * slots_out[num_tokens].  All or nothing: PA_ERR_OUT_OF_BLOCKS when the pool
+ * lacks free and cached blocks,
  * PA_ERR_UNSUPPORTED when the sequence would exceed max_blocks_per_seq blocks,
  * PA_ERR_INVALID_ARG for a bad seq, negative num_tokens or NULL slots_out (when
  * num_tokens > 0).  The context length afterwards counts the new tokens (the
@@ -80,8 +85,9 @@ pa_status pa_blocks_append(pa_blocks *bm, int seq, int num_tokens, int32_t *slot
  */
 pa_status pa_blocks_rollback(pa_blocks *bm, int seq, int num_tokens);
 
-/* pa_blocks_release -- the sequence is finished: all its blocks go back to the
- * free list and its context length becomes 0. */
+/* pa_blocks_release -- the sequence is finished: it lets all its blocks go (see
+ * prefix caching below: registered blocks stay in the prefix cache, the others
+ * return to the free list) and its context length becomes 0. */
 pa_status pa_blocks_release(pa_blocks *bm, int seq);
 
 /*
@@ -111,24 +117,34 @@ pa_status pa_blocks_tables(const pa_blocks *bm, const int32_t *seqs, int n, int3
                            int32_t *context_lens_out);
 
 /*
- * Prefix caching.  Physical blocks are reference counted: a block returns to the
- * free list when the last sequence holding it lets it go (release, preempt,
- * eviction, rollback).  Only full blocks are shared, so appends never write into
- * a shared block and no copy is ever needed.
+ * Prefix caching ("MicroGen", Key Features, "Prompt Prefix Caching"; "llminfer",
+ * Architecture: a prefix cache (LRU), and its prefix-reuse example, where a
+ * finished request's prompt serves the next one).  Physical blocks are reference
+ * counted.  When the last sequence holding a block lets it go (release,
+ * preempt, eviction, rollback), an unregistered block returns to the free list;
+ * a block registered under a prefix key stays in the prefix cache with its K/V
+ * and its key, so a later request with the same prefix finds it.  Allocations
+ * (pa_blocks_append) take free blocks first and then reclaim cached blocks,
+ * least recently let go first, dropping their keys; the blocks of one sequence
+ * enter the cache last block first, so a prefix loses its later blocks before
+ * its earlier ones.  free_blocks counts the free list only; append can use
+ * free_blocks + cached_blocks.  Only full blocks are shared, so appends never
+ * write into a shared block and no copy is ever needed.
  *
  * pa_blocks_publish -- register the first n_blocks blocks of seq, which must be
  * full (n_blocks * block_size <= its context) and not evicted, under the
  * caller's content keys keys[0..n_blocks-1] (for block i, a hash of every token
  * of the sequence up to the block's end, so that equal keys mean equal K/V).  A
- * key already registered keeps its block.  A block leaves the registry when it
- * is freed.
+ * key already registered keeps its block.  A block leaves the registry only when
+ * it is reclaimed.
  *
  * pa_blocks_attach_prefix -- for an empty sequence seq, attach the longest run
  * of registered blocks matching keys[0], keys[1], ... (stopping at the first key
- * not registered, or at max_blocks_per_seq): the sequence's table starts with
- * those blocks, each gaining a reference, and its context length becomes
- * (blocks attached) * block_size.  Returns the number of blocks attached (0 when
- * the first key misses), or -1 on a bad argument or a non-empty sequence.
+ * not registered, or at max_blocks_per_seq), whether other sequences hold them
+ * or they wait in the prefix cache: the sequence's table starts with those
+ * blocks, each gaining a reference, and its context length becomes (blocks
+ * attached) * block_size.  Returns the number of blocks attached (0 when the
+ * first key misses), or -1 on a bad argument or a non-empty sequence.
  */
 pa_status pa_blocks_publish(pa_blocks *bm, int seq, const uint64_t *keys, int n_blocks);
 int pa_blocks_attach_prefix(pa_blocks *bm, int seq, const uint64_t *keys, int n_blocks);

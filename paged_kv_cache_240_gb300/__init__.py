@@ -19,7 +19,7 @@ __all__ = [
     "pa_prefill_chunk",
     "pa_status_str", "pa_check_flags", "PA_FLAG_SLOT_RANGE", "PA_FLAG_BLOCK_ID",
     "PA_FLAG_CONTEXT_LEN", "PA_FLAG_Q_LEN", "PA_FLAG_TIMEOUT", "EXPORTED_SYMBOLS",
-    "pa_last_cuda_error",
+    "pa_last_cuda_error", "pa_selftest_bounded_wait",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpa_gb300.so")
@@ -38,7 +38,7 @@ EXPORTED_SYMBOLS = ("pa_write_kv", "pa_decode", "pa_decode_partitioned",
                     "pa_blocks_evict_window", "pa_blocks_tables", "pa_blocks_context_len",
                     "pa_blocks_get_stats", "pa_blocks_publish", "pa_blocks_attach_prefix",
                     "pa_linear_int8_quantize", "pa_linear_int8_workspace_bytes",
-                    "pa_linear_int8")
+                    "pa_linear_int8", "pa_selftest_bounded_wait")
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -82,8 +82,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_check_flags.argtypes = [ctypes.c_int32]
     lib.pa_last_cuda_error.argtypes = []
     lib.pa_last_cuda_error.restype = ctypes.c_char_p
+    lib.pa_selftest_bounded_wait.argtypes = [ctypes.c_longlong, P, P, P]
     for name in ("pa_write_kv", "pa_decode", "pa_decode_partitioned", "pa_decode_noalloc",
-                 "pa_prefill_chunk", "pa_check_flags"):
+                 "pa_prefill_chunk", "pa_check_flags", "pa_selftest_bounded_wait"):
         getattr(lib, name).restype = I
     if path == LIB_PATH:
         _lib = lib
@@ -260,3 +261,11 @@ def pa_prefill_chunk(cache: PagedCache, out, q, cu_q_lens, max_q_len, block_tabl
         int(cu_q_lens.shape[0]) - 1, int(q.shape[1]), _ptr(cu_q_lens), int(max_q_len),
         _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), float(sm_scale),
         int(window), None, 0, _ptr(err_flag), _stream(stream)), "pa_prefill_chunk")
+
+
+def pa_selftest_bounded_wait(limit_cycles, result, err_flag, stream=None):
+    """Run the bounded-wait self-check: result is a device int64 tensor [4]."""
+    _check_cuda(result, err_flag)
+    _raise(load_library().pa_selftest_bounded_wait(int(limit_cycles), _ptr(result),
+                                                   _ptr(err_flag), _stream(stream)),
+           "pa_selftest_bounded_wait")

@@ -15,7 +15,8 @@ class _Stats(ctypes.Structure):
                 ("preemptions", ctypes.c_longlong), ("recompute_tokens", ctypes.c_longlong),
                 ("evicted_blocks", ctypes.c_longlong), ("rolled_back_tokens", ctypes.c_longlong),
                 ("published_blocks", ctypes.c_longlong), ("prefix_hit_blocks", ctypes.c_longlong),
-                ("shared_blocks", ctypes.c_int)]
+                ("shared_blocks", ctypes.c_int), ("cached_blocks", ctypes.c_int),
+                ("revived_blocks", ctypes.c_longlong), ("reclaimed_blocks", ctypes.c_longlong)]
 
 
 def _lib():

@@ -18,8 +18,9 @@
 //   online softmax on S in the log2 domain, per row
 //   O += P V      A = P (f16/bf16), B = the block's 16 V rows (ldmatrix.trans)
 // For int8 caches the codes are turned into exact f16 integers in registers, the
-// K scale multiplies the scores and the V scale is folded into P, so dequantised
-// values are never materialised.
+// K scale multiplies the scores and the V scale goes into P as a value weight with
+// its own running reference (pa_device.cuh), so dequantised values are never
+// materialised.
 #pragma once
 
 #include <type_traits>
@@ -180,33 +181,63 @@ __device__ __forceinline__ void produce(const AttnParams& p, const void* tmk, co
 // a thread holds the four codes d = 16c+4t..16c+4t+3 of a row; the k-slots of
 // step c are mapped to those d (slots 2t,2t+1 -> d+0,1; slots 2t+8,2t+9 -> d+2,3)
 // and Q is laid out the same way (a dot product does not depend on the order).
+// int8 caches with bf16 q: each row is scaled by a power of two into f16 range
+// (q_prescale_shift); shift[r] receives that shift (0 otherwise).
 template <int MODE, int D, typename QT>
 __device__ __forceinline__ void load_q(uint32_t (&qa)[D / 16][4], const QT* row0, const QT* row1,
-                                       int t) {
+                                       int t, int (&shift)[2]) {
   const QT* rows[2] = {row0, row1};
+  shift[0] = shift[1] = 0;
+  if constexpr (MODE != kI8) {
 #pragma unroll
-  for (int ks = 0; ks < D / 16; ks++) {
+    for (int ks = 0; ks < D / 16; ks++)
 #pragma unroll
-    for (int r = 0; r < 2; r++) {
-      uint32_t lo = 0, hi = 0;
-      if (rows[r]) {
-        if constexpr (MODE != kI8) {
-          lo = *reinterpret_cast<const uint32_t*>(rows[r] + 16 * ks + 2 * t);
-          hi = *reinterpret_cast<const uint32_t*>(rows[r] + 16 * ks + 8 + 2 * t);
-        } else {
+      for (int r = 0; r < 2; r++) {
+        qa[ks][r] = rows[r] ? *reinterpret_cast<const uint32_t*>(rows[r] + 16 * ks + 2 * t) : 0u;
+        qa[ks][2 + r] =
+            rows[r] ? *reinterpret_cast<const uint32_t*>(rows[r] + 16 * ks + 8 + 2 * t) : 0u;
+      }
+  } else {
+    constexpr bool kBf16Q = !std::is_same<QT, __half>::value;
+    float mul[2] = {1.0f, 1.0f};
+    if constexpr (kBf16Q) {
+#pragma unroll
+      for (int r = 0; r < 2; r++) {
+        float amax = 0.0f;
+        if (rows[r]) {
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ks++) {
+            const uint2 raw = *reinterpret_cast<const uint2*>(rows[r] + 16 * ks + 4 * t);
+            const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
+#pragma unroll
+            for (int j = 0; j < 4; j++) amax = fmaxf(amax, fabsf(__bfloat162float(e[j])));
+          }
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        shift[r] = q_prescale_shift(amax);
+        mul[r] = pow2i(-shift[r]);
+      }
+    }
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ks++) {
+#pragma unroll
+      for (int r = 0; r < 2; r++) {
+        uint32_t lo = 0, hi = 0;
+        if (rows[r]) {
           const uint2 raw = *reinterpret_cast<const uint2*>(rows[r] + 16 * ks + 4 * t);
-          if constexpr (std::is_same<QT, __half>::value) {
+          if constexpr (!kBf16Q) {
             lo = raw.x;
             hi = raw.y;
           } else {
             const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
-            lo = pack_f16(__bfloat162float(e[0]), __bfloat162float(e[1]));
-            hi = pack_f16(__bfloat162float(e[2]), __bfloat162float(e[3]));
+            lo = pack_f16(__bfloat162float(e[0]) * mul[r], __bfloat162float(e[1]) * mul[r]);
+            hi = pack_f16(__bfloat162float(e[2]) * mul[r], __bfloat162float(e[3]) * mul[r]);
           }
         }
+        qa[ks][r] = lo;      // a0a1 / a2a3: rows gid / gid+8, first k pair
+        qa[ks][2 + r] = hi;  // a4a5 / a6a7: rows gid / gid+8, second k pair
       }
-      qa[ks][r] = lo;      // a0a1 / a2a3: rows gid / gid+8, first k pair
-      qa[ks][2 + r] = hi;  // a4a5 / a6a7: rows gid / gid+8, second k pair
     }
   }
 }
@@ -220,14 +251,19 @@ __device__ __forceinline__ int o_col(int nt, int n) {
 
 // One 16-token block through one warp's 16 rows.  pos0 is the logical position
 // of the block's first token; row r of this thread (gid, gid+8) sees keys in
-// [row_lo[r], row_hi[r]].  Tokens outside [keep_lo, keep_hi] may hold garbage
-// (tail slots, data before the window) and their V rows are zeroed before PV.
+// [row_lo[r], row_hi[r]] and its scores are scaled by rsc[r] (sm_scale * log2(e),
+// times the row's query prescale for int8 caches with bf16 q).  Tokens outside
+// [keep_lo, keep_hi] may hold garbage (tail slots, data before the window) and
+// their V rows are zeroed before PV (int8: their weight is 0 and codes are finite).
+// int8 caches: P is the value weight 2^(s + log2 v_scale - n[r]) of pa_device.cuh,
+// O is relative to the running reference n[r] and l to the softmax maximum m[r].
 template <int MODE, int D>
 __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], float (&o)[D / 8][4],
-                                             float (&m)[2], float (&l)[2], const uint8_t* stage,
-                                             const float* scales, int lane, int pos0,
-                                             const int (&row_lo)[2], const int (&row_hi)[2],
-                                             int keep_lo, int keep_hi, float scale_log2) {
+                                             float (&m)[2], float (&l)[2], float (&n)[2],
+                                             const uint8_t* stage, const float* scales, int lane,
+                                             int pos0, const int (&row_lo)[2],
+                                             const int (&row_hi)[2], int keep_lo, int keep_hi,
+                                             const float (&rsc)[2]) {
   using T = Tile<MODE, D>;
   constexpr bool BF = MODE == kBF16;
   const int t = lane & 3;
@@ -275,7 +311,7 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
       const int tok = 8 * nt + 2 * t + (i & 1);
       const int r = i >> 1;
       const int pos = pos0 + tok;
-      float x = s[nt][i] * scale_log2;
+      float x = s[nt][i] * rsc[r];
       if constexpr (MODE == kI8) x *= scales[tok];
       x = (pos >= row_lo[r] && pos <= row_hi[r]) ? x : -INFINITY;
       s[nt][i] = x;
@@ -292,31 +328,75 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
     m[r] = mn;
   }
   float ls[2] = {0.0f, 0.0f};
+  if constexpr (MODE != kI8) {
 #pragma unroll
-  for (int nt = 0; nt < 2; nt++)
+    for (int nt = 0; nt < 2; nt++)
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-      const float e = exp2f(s[nt][i] - ref[i >> 1]);
-      ls[i >> 1] += e;
-      if constexpr (MODE == kI8) {
-        const int tok = 8 * nt + 2 * t + (i & 1);
-        s[nt][i] = e > 0.0f ? e * scales[kBlock + tok] : 0.0f;  // V scale folded into P
-      } else {
+      for (int i = 0; i < 4; i++) {
+        const float e = exp2f(s[nt][i] - ref[i >> 1]);
+        ls[i >> 1] += e;
         s[nt][i] = e;
+      }
+#pragma unroll
+    for (int r = 0; r < 2; r++) l[r] = l[r] * corr[r] + ls[r];
+    // The running maximum rarely moves once a few blocks are in: skip the
+    // rescale when no row of the warp needs it.
+    if (!__all_sync(0xffffffffu, corr[0] == 1.0f && corr[1] == 1.0f)) {
+#pragma unroll
+      for (int nt = 0; nt < D / 8; nt++) {
+        o[nt][0] *= corr[0];
+        o[nt][1] *= corr[0];
+        o[nt][2] *= corr[1];
+        o[nt][3] *= corr[1];
+      }
+    }
+  } else {
+    // value weights: y = s + log2 v_scale (-inf where the row does not see the
+    // key, whatever its slot holds), relative to n, which moves up when a weight
+    // would pass 2^kLazyV
+    float lgv[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; nt++)
+#pragma unroll
+      for (int j = 0; j < 2; j++) {
+        const int pos = pos0 + 8 * nt + 2 * t + j;
+        lgv[nt][j] = pos >= keep_lo && pos <= keep_hi
+                         ? fast_log2(scales[kBlock + 8 * nt + 2 * t + j])
+                         : -INFINITY;
+      }
+    float y[2][4];
+    bool grow = false;
+#pragma unroll
+    for (int nt = 0; nt < 2; nt++)
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        const float e = exp2f(s[nt][i] - ref[i >> 1]);
+        ls[i >> 1] += e;
+        y[nt][i] = s[nt][i] + lgv[nt][i & 1];
+        grow |= y[nt][i] > n[i >> 1] + kLazyV;
+      }
+#pragma unroll
+    for (int r = 0; r < 2; r++) l[r] = l[r] * corr[r] + ls[r];
+    if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+      for (int r = 0; r < 2; r++) {
+        float ym = fmaxf(fmaxf(y[0][2 * r], y[0][2 * r + 1]), fmaxf(y[1][2 * r], y[1][2 * r + 1]));
+        ym = fmaxf(ym, __shfl_xor_sync(0xffffffffu, ym, 1));
+        ym = fmaxf(ym, __shfl_xor_sync(0xffffffffu, ym, 2));
+        const float nn = fmaxf(n[r], ym);
+        const float f = fast_exp2(n[r] - nn);
+        n[r] = nn;
+#pragma unroll
+        for (int nt = 0; nt < D / 8; nt++) {
+          o[nt][2 * r] *= f;
+          o[nt][2 * r + 1] *= f;
+        }
       }
     }
 #pragma unroll
-  for (int r = 0; r < 2; r++) l[r] = l[r] * corr[r] + ls[r];
-  // The running maximum rarely moves once a few blocks are in: skip the
-  // rescale when no row of the warp needs it.
-  if (!__all_sync(0xffffffffu, corr[0] == 1.0f && corr[1] == 1.0f)) {
+    for (int nt = 0; nt < 2; nt++)
 #pragma unroll
-    for (int nt = 0; nt < D / 8; nt++) {
-      o[nt][0] *= corr[0];
-      o[nt][1] *= corr[0];
-      o[nt][2] *= corr[1];
-      o[nt][3] *= corr[1];
-    }
+      for (int i = 0; i < 4; i++) s[nt][i] = fast_exp2(y[nt][i] - n[i >> 1]);
   }
   uint32_t pa[4];
   pa[0] = pack2<BF>(s[0][0], s[0][1]);  // row gid,   tokens 2t, 2t+1

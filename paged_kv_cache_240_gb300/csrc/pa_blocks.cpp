@@ -4,7 +4,10 @@
 // accounting, recomputation counters after preemption; "MicroGen", Key
 // Features: logical-to-physical block mapping, sliding window eviction, KV
 // cache state rollback; "Prompt Prefix Caching": token sequence hashing with
-// sub-sequence prefix lookup).  Plain C++ on the host; the C ABI is pa_blocks.h.
+// sub-sequence prefix lookup; "llminfer", Architecture: a prefix cache (LRU),
+// and its prefix-reuse example, where a finished request's prompt blocks serve
+// the next request with the same prompt).  Plain C++ on the host; the C ABI is
+// pa_blocks.h.
 #include "pa_blocks.h"
 
 #include <algorithm>
@@ -22,6 +25,13 @@ struct pa_blocks {
   std::vector<uint64_t> key_of;     // the prefix key a block is registered under
   std::vector<uint8_t> keyed;       // whether it is registered
   std::unordered_map<uint64_t, int32_t> registry;  // prefix key -> block
+  // The prefix cache: registered blocks that no sequence holds any more keep
+  // their K/V and their key, on a list ordered by when they were let go (least
+  // recently used at the head).  An allocation takes a free block first, and
+  // reclaims the head of this list only when none is left.
+  std::vector<int32_t> lru_prev, lru_next;  // intrusive list links, -1 = none
+  int32_t lru_head = -1, lru_tail = -1;
+  int cached = 0;
   pa_blocks_stats stats;
 
   int32_t* table(int seq) { return tables.data() + (size_t)seq * max_blocks_per_seq; }
@@ -32,28 +42,65 @@ struct pa_blocks {
   int blocks_for(long long tokens) const {
     return (int)((tokens + block_size - 1) / block_size);
   }
+  // Blocks an allocation can take: free ones and cached ones.
+  long long available() const { return (long long)free_stack.size() + cached; }
+
+  void lru_push_back(int32_t b) {  // b becomes the most recently used
+    lru_prev[b] = lru_tail;
+    lru_next[b] = -1;
+    if (lru_tail >= 0) lru_next[lru_tail] = b;
+    else lru_head = b;
+    lru_tail = b;
+    cached++;
+  }
+  void lru_remove(int32_t b) {
+    if (lru_prev[b] >= 0) lru_next[lru_prev[b]] = lru_next[b];
+    else lru_head = lru_next[b];
+    if (lru_next[b] >= 0) lru_prev[lru_next[b]] = lru_prev[b];
+    else lru_tail = lru_prev[b];
+    lru_prev[b] = lru_next[b] = -1;
+    cached--;
+  }
+  // A block for a new position: the top of the free list, else the least
+  // recently used cached block, whose key is dropped.  The caller has checked
+  // available() > 0.
   int32_t pop_free() {
-    const int32_t b = free_stack.back();
-    free_stack.pop_back();
+    int32_t b;
+    if (!free_stack.empty()) {
+      b = free_stack.back();
+      free_stack.pop_back();
+    } else {
+      b = lru_head;
+      lru_remove(b);
+      registry.erase(key_of[b]);
+      keyed[b] = 0;
+      stats.reclaimed_blocks++;
+    }
     refs[b] = 1;
     return b;
   }
-  // One holder lets block b go; the last one returns it to the free list.
+  // One holder lets block b go.  The last one returns it to the free list, or,
+  // if it is registered under a prefix key, to the tail of the prefix cache.
   void push_free(int32_t b) {
     if (--refs[b] > 0) {
       if (refs[b] == 1) stats.shared_blocks--;
       return;
     }
-    if (keyed[b]) {
-      registry.erase(key_of[b]);
-      keyed[b] = 0;
-    }
-    free_stack.push_back(b);
+    if (keyed[b]) lru_push_back(b);
+    else free_stack.push_back(b);
   }
-  // Return logical blocks [from, to) of seq to the free list (skipping holes).
+  // Return logical blocks [from, to) of seq (skipping holes).  Unregistered
+  // blocks go to the free list in table order; registered ones go to the cache
+  // last block first, so that a prefix's later blocks are reclaimed before its
+  // earlier ones (a prefix is found from its first block on).
   void free_range(int seq, int from, int to) {
     int32_t* t = table(seq);
     for (int i = from; i < to; i++)
+      if (t[i] >= 0 && !(keyed[t[i]] && refs[t[i]] == 1)) {
+        push_free(t[i]);
+        t[i] = -1;
+      }
+    for (int i = to - 1; i >= from; i--)
       if (t[i] >= 0) {
         push_free(t[i]);
         t[i] = -1;
@@ -92,6 +139,8 @@ extern "C" pa_blocks* pa_blocks_create(int num_blocks, int block_size, int max_s
     bm->refs.assign(num_blocks, 0);
     bm->key_of.assign(num_blocks, 0);
     bm->keyed.assign(num_blocks, 0);
+    bm->lru_prev.assign(num_blocks, -1);
+    bm->lru_next.assign(num_blocks, -1);
   } catch (...) {
     delete bm;
     return nullptr;
@@ -110,7 +159,7 @@ extern "C" pa_status pa_blocks_append(pa_blocks* bm, int seq, int num_tokens,
   const long long L = bm->lens[seq], L2 = L + num_tokens;
   const int have = bm->blocks_for(L), need = bm->blocks_for(L2);
   if (need > bm->max_blocks_per_seq) return PA_ERR_UNSUPPORTED;
-  if (need - have > (int)bm->free_stack.size()) return PA_ERR_OUT_OF_BLOCKS;
+  if (need - have > bm->available()) return PA_ERR_OUT_OF_BLOCKS;
   int32_t* t = bm->table(seq);
   for (int i = have; i < need; i++) t[i] = bm->pop_free();
   for (int k = 0; k < num_tokens; k++) {
@@ -233,6 +282,10 @@ extern "C" int pa_blocks_attach_prefix(pa_blocks* bm, int seq, const uint64_t* k
     const auto hit = bm->registry.find(keys[k]);
     if (hit == bm->registry.end()) break;
     const int32_t b = hit->second;
+    if (bm->refs[b] == 0) {  // in the prefix cache: revived
+      bm->lru_remove(b);
+      bm->stats.revived_blocks++;
+    }
     if (++bm->refs[b] == 2) bm->stats.shared_blocks++;
     t[k] = b;
   }
@@ -254,5 +307,6 @@ extern "C" pa_status pa_blocks_get_stats(const pa_blocks* bm, pa_blocks_stats* o
   if (!bm || !out) return PA_ERR_INVALID_ARG;
   *out = bm->stats;
   out->free_blocks = (int)bm->free_stack.size();
+  out->cached_blocks = bm->cached;
   return PA_OK;
 }

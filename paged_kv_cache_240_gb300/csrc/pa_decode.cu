@@ -31,29 +31,50 @@ constexpr int kDecHeads = 8;
 // Q^T -> B fragments: thread (g, t) holds head g.  Same d order as the K tile
 // fragments: natural for 16-bit caches; for int8 the thread's four codes of
 // a k-step are d = 16c+4t..16c+4t+3 (slots 2t,2t+1 -> d+0,1; 2t+8,2t+9 -> d+2,3).
+// int8 caches with bf16 q: the head's row is scaled by a power of two into f16
+// range (q_prescale_shift); returns that shift (0 otherwise), the same for the
+// four lanes that hold a head.
 template <int MODE, int D, typename QT>
-__device__ __forceinline__ void load_qt(uint32_t (&qb)[D / 16][2], const QT* row, int t) {
+__device__ __forceinline__ int load_qt(uint32_t (&qb)[D / 16][2], const QT* row, int t) {
+  if constexpr (MODE != kI8) {
 #pragma unroll
-  for (int ks = 0; ks < D / 16; ks++) {
-    uint32_t lo = 0, hi = 0;
-    if (row) {
-      if constexpr (MODE != kI8) {
-        lo = *reinterpret_cast<const uint32_t*>(row + 16 * ks + 2 * t);
-        hi = *reinterpret_cast<const uint32_t*>(row + 16 * ks + 8 + 2 * t);
-      } else {
-        const uint2 raw = *reinterpret_cast<const uint2*>(row + 16 * ks + 4 * t);
-        if constexpr (std::is_same<QT, __half>::value) {
-          lo = raw.x;
-          hi = raw.y;
-        } else {
-          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
-          lo = pack_f16(__bfloat162float(e[0]), __bfloat162float(e[1]));
-          hi = pack_f16(__bfloat162float(e[2]), __bfloat162float(e[3]));
-        }
-      }
+    for (int ks = 0; ks < D / 16; ks++) {
+      qb[ks][0] = row ? *reinterpret_cast<const uint32_t*>(row + 16 * ks + 2 * t) : 0u;
+      qb[ks][1] = row ? *reinterpret_cast<const uint32_t*>(row + 16 * ks + 8 + 2 * t) : 0u;
     }
-    qb[ks][0] = lo;
-    qb[ks][1] = hi;
+    return 0;
+  } else {
+    uint2 raw[D / 16];
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ks++)
+      raw[ks] = row ? *reinterpret_cast<const uint2*>(row + 16 * ks + 4 * t) : make_uint2(0, 0);
+    if constexpr (std::is_same<QT, __half>::value) {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ks++) {
+        qb[ks][0] = raw[ks].x;
+        qb[ks][1] = raw[ks].y;
+      }
+      return 0;
+    } else {
+      float amax = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ks++) {
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[ks]);
+#pragma unroll
+        for (int j = 0; j < 4; j++) amax = fmaxf(amax, fabsf(__bfloat162float(e[j])));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      const int shift = q_prescale_shift(amax);
+      const float mul = pow2i(-shift);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ks++) {
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[ks]);
+        qb[ks][0] = pack_f16(__bfloat162float(e[0]) * mul, __bfloat162float(e[1]) * mul);
+        qb[ks][1] = pack_f16(__bfloat162float(e[2]) * mul, __bfloat162float(e[3]) * mul);
+      }
+      return shift;
+    }
   }
 }
 
@@ -67,19 +88,23 @@ __device__ __forceinline__ int ot_col(int mt, int g, int r) {
 // One 16-token block through one warp: the thread's two heads are 2t, 2t+1.
 // Keys at positions outside [lo, hi] are masked; their V rows may hold garbage
 // (tail slots, data before the window) and are zeroed before O^T += V^T P^T.
+// hsc[c] is head 2t+c's score scale (sm_scale * log2(e), times the query's
+// prescale 2^shift for int8 caches with bf16 q).
 //
 // int8 caches: the MMAs see each code as the exact f16 integer code + 1152, so
 // S^T comes out high by 1152 * sum_d q[h][d] (kcorr, per head, subtracted here)
-// and O^T high by 1152 * sum_j P'[j][h], where P' = P * v_scale rounded to f16
-// as the MMA sees it; that sum is kept in lv with the same online rescaling as
-// O^T and subtracted once at the end.
+// and O^T high by 1152 * sum_j P'[j][h], where P'[j][h] = 2^(y_j - n_h) is the
+// value weight of pa_device.cuh (y_j = s_j + log2 v_scale_j, n the running
+// reference) rounded to f16 as the MMA sees it; that sum is kept in lv with the
+// same rescaling as O^T and subtracted once at the end.  O^T and lv are
+// relative to n, the normaliser l to the softmax maximum m.
 template <int MODE, int D>
 __device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2],
                                                  float (&o)[D / 16][4], float (&m)[2],
-                                                 float (&l)[2], float (&lv)[2],
+                                                 float (&l)[2], float (&n)[2], float (&lv)[2],
                                                  const float (&kcorr)[2], const uint8_t* stage,
                                                  const float* scales, int lane, int pos0, int lo,
-                                                 int hi, float scale_log2) {
+                                                 int hi, const float (&hsc)[2]) {
   using T = Tile<MODE, D>;
   constexpr bool BF = MODE == kBF16;
   const int g = lane >> 2, t = lane & 3;
@@ -112,15 +137,20 @@ __device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2]
   }
 
   // ---- scale, mask, online softmax over tokens (log2 domain); i: token g+8(i>>1), head 2t+(i&1)
+  bool kept[2];
+#pragma unroll
+  for (int r = 0; r < 2; r++) {
+    const int pos = pos0 + g + 8 * r;
+    kept[r] = pos >= lo && pos <= hi;
+  }
   float s[4], mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
   for (int i = 0; i < 4; i++) {
     const int tok = g + 8 * (i >> 1);
-    const int pos = pos0 + tok;
     float x;
-    if constexpr (MODE == kI8) x = (sa[i] + sb[i] - kcorr[i & 1]) * (scale_log2 * scales[tok]);
-    else x = (sa[i] + sb[i]) * scale_log2;
-    x = (pos >= lo && pos <= hi) ? x : -INFINITY;
+    if constexpr (MODE == kI8) x = (sa[i] + sb[i] - kcorr[i & 1]) * (hsc[i & 1] * scales[tok]);
+    else x = (sa[i] + sb[i]) * hsc[i & 1];
+    x = kept[i >> 1] ? x : -INFINITY;
     s[i] = x;
     mx[i & 1] = fmaxf(mx[i & 1], x);
   }
@@ -140,17 +170,51 @@ __device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2]
   for (int i = 0; i < 4; i++) {
     const float e = fast_exp2(s[i] - ref[i & 1]);
     l[i & 1] = (i < 2 ? l[i & 1] * corr[i & 1] : l[i & 1]) + e;
-    if constexpr (MODE == kI8) p[i] = e > 0.0f ? e * scales[kBlock + g + 8 * (i >> 1)] : 0.0f;
-    else p[i] = e;
+    p[i] = e;
   }
-  if (!__all_sync(0xffffffffu, corr[0] == 1.0f && corr[1] == 1.0f)) {
+  if constexpr (MODE != kI8) {
+    if (!__all_sync(0xffffffffu, corr[0] == 1.0f && corr[1] == 1.0f)) {
 #pragma unroll
-    for (int mt = 0; mt < D / 16; mt++) {
-      o[mt][0] *= corr[0];
-      o[mt][1] *= corr[1];
-      o[mt][2] *= corr[0];
-      o[mt][3] *= corr[1];
+      for (int mt = 0; mt < D / 16; mt++) {
+        o[mt][0] *= corr[0];
+        o[mt][1] *= corr[1];
+        o[mt][2] *= corr[0];
+        o[mt][3] *= corr[1];
+      }
     }
+  } else {
+    // value weights 2^(y - n), y = s + log2 v_scale (-inf for a masked token,
+    // whatever its slot holds); n moves up when a weight would pass 2^kLazyV
+    float lgv[2], y[4];
+#pragma unroll
+    for (int r = 0; r < 2; r++)
+      lgv[r] = kept[r] ? fast_log2(scales[kBlock + g + 8 * r]) : -INFINITY;
+    bool grow = false;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      y[i] = s[i] + lgv[i >> 1];
+      grow |= y[i] > n[i & 1] + kLazyV;
+    }
+    if (__any_sync(0xffffffffu, grow)) {
+      float ym[2] = {fmaxf(y[0], y[2]), fmaxf(y[1], y[3])};
+#pragma unroll
+      for (int c = 0; c < 2; c++) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1)
+          ym[c] = fmaxf(ym[c], __shfl_xor_sync(0xffffffffu, ym[c], off));
+        const float nn = fmaxf(n[c], ym[c]);
+        const float f = fast_exp2(n[c] - nn);
+        n[c] = nn;
+        lv[c] *= f;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; mt++) {
+          o[mt][c] *= f;
+          o[mt][c + 2] *= f;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; i++) p[i] = fast_exp2(y[i] - n[i & 1]);
   }
   // P^T as the PV B operand: C tile (token g, heads 2t, 2t+1) transposed to
   // (head g, tokens 2t, 2t+1), once for tokens 0..7 and once for 8..15.
@@ -158,8 +222,8 @@ __device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2]
   if constexpr (MODE == kI8) {
     const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&pk0));
     const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&pk1));
-    lv[0] = lv[0] * corr[0] + (f0.x + f1.x);
-    lv[1] = lv[1] * corr[1] + (f0.y + f1.y);
+    lv[0] += f0.x + f1.x;
+    lv[1] += f0.y + f1.y;
   }
   const uint32_t pb0 = movmatrix_t(pk0);
   const uint32_t pb1 = movmatrix_t(pk1);
@@ -329,17 +393,25 @@ __global__ void __launch_bounds__(kDecThreads, MODE == kI8 ? 5 : 3)
   const int g = lane >> 2, t = lane & 3;
   const QT* q = static_cast<const QT*>(p.q);
   uint32_t qb[D / 16][2];
-  load_qt<MODE, D, QT>(qb, g < rows ? q + ((long long)b * p.num_q_heads + h0 + g) * D : nullptr,
-                       t);
+  const int qshift = load_qt<MODE, D, QT>(
+      qb, g < rows ? q + ((long long)b * p.num_q_heads + h0 + g) * D : nullptr, t);
+  // score scale of this thread's score columns (heads 2t, 2t+1; lane 8t+4c holds head 2t+c)
+  float hsc[2] = {p.scale_log2, p.scale_log2};
+  if constexpr (MODE == kI8 && !std::is_same<QT, __half>::value) {
+#pragma unroll
+    for (int c = 0; c < 2; c++)
+      hsc[c] = p.scale_log2 * pow2i(__shfl_sync(0xffffffffu, qshift, 8 * t + 4 * c));
+  }
   float o[D / 16][4];
 #pragma unroll
   for (int mt = 0; mt < D / 16; mt++)
 #pragma unroll
     for (int i = 0; i < 4; i++) o[mt][i] = 0.0f;
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f}, lv[2] = {0.0f, 0.0f};
+  float n[2] = {kNoRef, kNoRef};  // int8: the value weights' reference
   float kcorr[2] = {0.0f, 0.0f};
   if constexpr (MODE == kI8) {
-    // 1152 * sum_d q[h][d] for this thread's score columns h = 2t, 2t+1
+    // 1152 * sum_d q[h][d] (the f16 q the MMA sees) for this thread's score columns h = 2t, 2t+1
     float qs = 0.0f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ks++)
@@ -363,10 +435,10 @@ __global__ void __launch_bounds__(kDecThreads, MODE == kI8 ? 5 : 3)
       break;
     }
     if (s.valid[slot])
-      attend_block_dec<MODE, D>(qb, o, m, l, lv, kcorr,
+      attend_block_dec<MODE, D>(qb, o, m, l, n, lv, kcorr,
                                 s.stages + slot * Tile<MODE, D>::kStageBytes,
                                 s.scales + slot * 2 * kBlock, lane,
-                                (blk0 + warp + kDecWarps * k) * kBlock, lo, L - 1, p.scale_log2);
+                                (blk0 + warp + kDecWarps * k) * kBlock, lo, L - 1, hsc);
     __syncwarp();
     if (k + 2 < nmine) {
       if (((k + 2) & 31) == 0)  // next 32 of this warp's block ids
@@ -390,11 +462,16 @@ __global__ void __launch_bounds__(kDecThreads, MODE == kI8 ? 5 : 3)
       l[c] += __shfl_xor_sync(0xffffffffu, l[c], off);
       if constexpr (MODE == kI8) lv[c] += __shfl_xor_sync(0xffffffffu, lv[c], off);
     }
-  if constexpr (MODE == kI8) {  // remove the 1152 carried by every V code
+  if constexpr (MODE == kI8) {
+    // remove the 1152 carried by every V code, then move O^T from the value
+    // weights' reference n to the softmax's m (fp32; no key seen: m = -inf, O^T = 0)
+    float f[2];
+#pragma unroll
+    for (int c = 0; c < 2; c++) f[c] = m[c] == -INFINITY ? 0.0f : exp2f(n[c] - m[c]);
 #pragma unroll
     for (int mt = 0; mt < D / 16; mt++)
 #pragma unroll
-      for (int i = 0; i < 4; i++) o[mt][i] -= 1152.0f * lv[i & 1];
+      for (int i = 0; i < 4; i++) o[mt][i] = (o[mt][i] - 1152.0f * lv[i & 1]) * f[i & 1];
   }
   __syncthreads();  // every stage consumed: reuse them for the merge
   if (*s.abort_flag) return;
@@ -715,7 +792,38 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRA
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices];  // device address of the scratch, per device ordinal
+void* g_noalloc_addr[kMaxDevices];                // device address of the scratch, per device
+unsigned long long g_noalloc_ctx[kMaxDevices];    // id of the context it was looked up in
+
+// Unique id of the calling thread's current context (0 if the driver cannot say).
+// A device reset ends the context the cached address belongs to; the next call
+// sees a new id and looks the address up again.
+unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = []() -> GetCurrentFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<GetCurrentFn>(f);
+  }();
+  static GetIdFn get_id = []() -> GetIdFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<GetIdFn>(f);
+  }();
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 pa_status noalloc_scratch(void** addr) {
   int dev = -1;
@@ -723,12 +831,23 @@ pa_status noalloc_scratch(void** addr) {
   if (e != cudaSuccess) return pa_internal::cuda_status(e);
   if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
+  if (!g_noalloc_addr[dev]) {  // first call on this device: the runtime makes its context
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr)
       return pa_internal::cuda_status(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
     g_noalloc_addr[dev] = p;
+    g_noalloc_ctx[dev] = current_context_id();
+  } else {
+    const unsigned long long id = current_context_id();
+    if (id != g_noalloc_ctx[dev]) {  // the device was reset since: look it up again
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess || p == nullptr)
+        return pa_internal::cuda_status(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+      g_noalloc_addr[dev] = p;
+      g_noalloc_ctx[dev] = current_context_id();  // the lookup may have made the context
+    }
   }
   *addr = g_noalloc_addr[dev];
   return PA_OK;

@@ -96,12 +96,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete; false if the time
-// limit ran out first.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// limit (SM clock cycles) ran out first.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
   return true;
 }
@@ -285,6 +286,46 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// log2(x) with the hardware approximation (absolute error near 2^-22; 0 -> -inf;
+// subnormal inputs are not flushed).
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------------------ int8 value weights
+//
+// An int8 cache row's values are code * v_scale, with v_scale = amax / 127 of
+// that row ("MicroGen", Key Features: dynamic INT8 KV quantisation with a vector
+// scale), so rows of very different magnitudes share one sequence.  The P V
+// product takes the softmax weight and the row's scale together as one 16-bit
+// MMA operand, w_j = 2^(s_j - m) * v_scale_j.  Folding v_scale into a weight
+// that is at most 1 underflows f16 (below 2^-14 it loses bits, below 2^-24 it is
+// 0) once the rows are small, so the weights are taken relative to their own
+// running reference instead: with y_j = s_j + log2(v_scale_j) and a per-row
+// reference n (the largest y_j seen when it was last moved), the operand is
+// 2^(y_j - n), at most 2^kLazyV, and the largest term of the sum is at least 1.
+// The accumulated O therefore carries the factor 2^-n; it is rescaled only when
+// some y_j exceeds n by more than kLazyV, and converted to the softmax's
+// reference m once, in fp32, at the end (O * 2^(n - m)).  The error of every
+// term is then relative to the largest term, whatever the rows' magnitudes.
+constexpr float kLazyV = 8.0f;
+constexpr float kNoRef = -3.402823466e38f;  // n before any weight: y - n stays -inf for y = -inf
+
+// bf16 query values reach 3.4e38, f16 operands only 65504.  A query row whose
+// largest |q| is 2^E (E >= 15) is multiplied by 2^-(E - 14) before it is
+// narrowed to f16 (a power of two: every bit of the bf16 values that matters to
+// the fp32 dot product survives) and the score by 2^(E - 14) after the MMA.
+// Returns that exponent shift (0 when the row already fits).
+__device__ __forceinline__ int q_prescale_shift(float amax) {
+  const int e = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+  return e > 14 ? e - 14 : 0;
+}
+__device__ __forceinline__ float pow2i(int k) {  // 2^k for -126 <= k <= 127
+  return __uint_as_float((uint32_t)(k + 127) << 23);
 }
 
 // ------------------------------------------------------------------ misc

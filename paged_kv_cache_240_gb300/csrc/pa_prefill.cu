@@ -99,13 +99,16 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   uint32_t qa[D / 16][4];
-  load_q<MODE, D, QT>(qa, qrow[0], qrow[1], t);
+  int qshift[2];
+  load_q<MODE, D, QT>(qa, qrow[0], qrow[1], t, qshift);
+  const float rsc[2] = {p.scale_log2 * pow2i(qshift[0]), p.scale_log2 * pow2i(qshift[1])};
   float o[D / 8][4];
 #pragma unroll
   for (int nt = 0; nt < D / 8; nt++)
 #pragma unroll
     for (int i = 0; i < 4; i++) o[nt][i] = 0.0f;
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
+  float nref[2] = {kNoRef, kNoRef};  // int8: the value weights' reference
 
   bool timed_out = false;
   for (int i = 0; i < nblk; i++) {
@@ -117,9 +120,9 @@ __global__ void __launch_bounds__(kThreads)
     }
     const int pos0 = (first + i) * kBlock;
     if (s.valid[slot] && pos0 <= whi && pos0 + kBlock - 1 >= wlo)
-      attend_block<MODE, D>(qa, o, m, l, s.stages + slot * Tile<MODE, D>::kStageBytes,
+      attend_block<MODE, D>(qa, o, m, l, nref, s.stages + slot * Tile<MODE, D>::kStageBytes,
                             s.scales + slot * 2 * kBlock, lane, pos0,
-                            row_lo, row_hi, lo_u, hi_u, p.scale_log2);
+                            row_lo, row_hi, lo_u, hi_u, rsc);
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.empty[slot]);
   }
@@ -133,7 +136,9 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
   for (int r = 0; r < 2; r++) {
     if (orow[r] < 0) continue;
-    const float inv = l[r] > 0.0f ? 1.0f / l[r] : 0.0f;
+    // int8: O is relative to the value weights' reference, l to m
+    float inv = l[r] > 0.0f ? 1.0f / l[r] : 0.0f;
+    if constexpr (MODE == kI8) inv = l[r] > 0.0f ? exp2f(nref[r] - m[r]) / l[r] : 0.0f;
     QT* dst = out + orow[r] * D;
 #pragma unroll
     for (int nt = 0; nt < D / 8; nt++) {

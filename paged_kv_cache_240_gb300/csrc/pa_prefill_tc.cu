@@ -484,7 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     sched[4] = 0x7fffffff;
     fence_mbar_init();
   }
-  if (warp == 1) {  // tensor memory: per query tile, S (P in its first half) and O
+  // Tensor memory: per query tile, S (P in its first half) and O -- all 512
+  // columns of the SM.  The allocation does not wait on another CTA of this
+  // launch: the 231.6 KB of dynamic shared memory leaves room for one CTA per SM,
+  // and the library's other kernels allocate no tensor memory.
+  if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(LY::kTmemCols));
@@ -655,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&k_full[t % kKS], (t / kKS) & 1)) break;
         for (int t = gv > VS ? gv - VS : 0; t < gv; t++)
           if (!mbar_wait(&v_full[t % VS], (t / VS) & 1)) break;
-        if (k > 0) mbar_wait(q_full, (k - 1) & 1);
+        if (k > 0 && !mbar_wait(q_full, (k - 1) & 1)) timed_out = true;
       }
       if (timed_out && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
     } else if (warp == 2) {

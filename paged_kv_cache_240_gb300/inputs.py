@@ -200,6 +200,24 @@ def f32_to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(dtype)
 
 
+def bits_to_f32(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """fp16 or bf16 bit patterns -> float32 (exact)."""
+    bits = np.ascontiguousarray(bits, np.uint16)
+    if dtype == "f16":
+        return bits.view(np.float16).astype(np.float32)
+    if dtype == "bf16":
+        return (bits.astype(np.uint32) << 16).view(np.float32)
+    raise ValueError(dtype)
+
+
+def scaled_bits(bits: np.ndarray, dtype: str, factor) -> np.ndarray:
+    """Draws of another magnitude: the values of ``bits`` times ``factor`` (a
+    scalar, or an array broadcast against the rows, e.g. one factor per token),
+    rounded back to ``dtype``."""
+    x = bits_to_f32(bits, dtype).astype(np.float64) * np.asarray(factor, np.float64)
+    return f32_to_bits(x.astype(np.float32), dtype)
+
+
 def normal_bits(shape, dtype: str, seed: int, stream: int) -> np.ndarray:
     rng = np.random.default_rng([seed, 100 + stream])
     return f32_to_bits(rng.standard_normal(size=shape, dtype=np.float32), dtype)

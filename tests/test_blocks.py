@@ -27,7 +27,7 @@ def check_invariants(bm, nseq, shared_ok=False):
     if not shared_ok:
         assert distinct == owned.size, "a block in two places"
     assert st["shared_blocks"] == owned.size - distinct or shared_ok
-    assert distinct + st["free_blocks"] == st["num_blocks"]
+    assert distinct + st["free_blocks"] + st["cached_blocks"] == st["num_blocks"]
     assert st["tokens_held"] == int(lens.sum())
     assert st["live_seqs"] == int((lens > 0).sum())
     for s in range(nseq):
@@ -271,9 +271,236 @@ def test_prefix_blocks_are_shared_and_reference_counted():
     free_before = bm.stats()["free_blocks"]
     bm.release(0)                         # the shared blocks stay alive for sequence 1
     st = bm.stats()
-    assert st["shared_blocks"] == 0 and st["free_blocks"] == free_before + 2
-    assert bm.attach_prefix(3, keys) == 2  # still registered: held by sequence 1
+    # its third prompt block is cached (keyed, no holder), its partial block freed
+    assert st["shared_blocks"] == 0 and st["free_blocks"] == free_before + 1
+    assert st["cached_blocks"] == 1
+    assert bm.attach_prefix(3, keys) == 3  # two held by sequence 1, one revived
+    assert bm.stats()["revived_blocks"] == 1
     bm.release(1)
-    bm.release(3)                         # last holders gone: blocks and keys freed
-    assert bm.stats()["free_blocks"] == 12
-    assert bm.attach_prefix(2, keys) == 0
+    bm.release(3)                         # last holders gone: the keyed blocks are cached
+    st = bm.stats()
+    assert st["free_blocks"] == 9 and st["cached_blocks"] == 3
+    assert bm.attach_prefix(2, keys) == 3 and bm.stats()["revived_blocks"] == 4
+
+
+def test_prefix_outlives_its_request():
+    """"llminfer", Prefix KV cache reuse: request r1 runs to completion, then r2
+    with the same prompt finds r1's prompt blocks in the prefix cache."""
+    bm = BlockManager(num_blocks=20, block_size=16, max_seqs=2, max_blocks_per_seq=8)
+    bm.append(0, 40)                      # r1's prompt: 2 full blocks + 8 tokens
+    keys = np.array([11, 22], np.uint64)
+    bm.publish(0, keys)
+    bm.append(0, 5)                       # r1 decodes
+    tab1, _ = bm.tables([0])
+    bm.release(0)                         # r1 finishes
+    st = bm.stats()
+    assert st["cached_blocks"] == 2 and st["free_blocks"] == 18 and st["live_seqs"] == 0
+    assert bm.attach_prefix(1, keys) == 2  # r2: a hit on both prompt blocks
+    tab2, lens2 = check_invariants(bm, 2)
+    assert (tab2[1, :2] == tab1[0, :2]).all() and lens2[1] == 32
+    st = bm.stats()
+    assert st["prefix_hit_blocks"] == 2 and st["revived_blocks"] == 2
+    assert st["cached_blocks"] == 0 and st["reclaimed_blocks"] == 0
+    new = bm.append(1, 8)                 # r2's own tokens go to a fresh block
+    assert not np.isin(new // 16, tab1[0, :2]).any()
+
+
+def test_prefix_cache_is_reclaimed_under_pressure_lru_first():
+    """With no free block left, appends take cached blocks back, least recently
+    let go first; a prefix loses its later blocks before its first."""
+    bm = BlockManager(num_blocks=8, block_size=4, max_seqs=3, max_blocks_per_seq=10)
+    bm.append(0, 12)                      # prompt A: blocks 0, 1, 2
+    bm.publish(0, np.array([1, 2, 3], np.uint64))
+    bm.append(1, 8)                       # prompt B: blocks 3, 4
+    bm.publish(1, np.array([7, 8], np.uint64))
+    tab, _ = bm.tables([0, 1])
+    bm.release(0)                         # A let go first (least recent), then B
+    bm.release(1)
+    st = bm.stats()
+    assert st["cached_blocks"] == 5 and st["free_blocks"] == 3
+    with pytest.raises(pa.PaError) as e:
+        bm.append(2, 4 * 9)               # more than free + cached
+    assert e.value.status == pa.PA_ERR_OUT_OF_BLOCKS
+    bm.append(2, 4 * 5)                   # 3 free + 2 reclaimed: A's blocks 2, then 1
+    st = bm.stats()
+    assert st["reclaimed_blocks"] == 2 and st["cached_blocks"] == 3
+    t2, _ = bm.tables([2])
+    assert set(t2[0, 3:5].tolist()) == {int(tab[0, 2]), int(tab[0, 1])}
+    assert bm.attach_prefix(0, np.array([1, 2, 3], np.uint64)) == 1   # only A's head left
+    assert bm.attach_prefix(1, np.array([7, 8], np.uint64)) == 2      # B untouched
+    check_invariants(bm, 3, shared_ok=True)
+
+
+class PrefixModel(Model):
+    """The header's contract with prefix caching: reference counts, a registry of
+    keys and a least-recently-used list of cached blocks."""
+
+    def __init__(self, *a):
+        super().__init__(*a)
+        self.refs, self.key_of, self.registry, self.lru = {}, {}, {}, []
+        self.reclaimed = self.revived = 0
+
+    def pop(self):
+        if self.free:
+            b = self.free.pop()
+        else:
+            b = self.lru.pop(0)
+            del self.registry[self.key_of.pop(b)]
+            self.reclaimed += 1
+        self.refs[b] = 1
+        return b
+
+    def let_go(self, b):
+        self.refs[b] -= 1
+        if self.refs[b] == 0:
+            (self.lru if b in self.key_of else self.free).append(b)
+
+    def release_range(self, s, lo, hi):
+        t = self.tab[s]
+        order = [i for i in range(lo, hi) if t[i] >= 0 and not (
+            t[i] in self.key_of and self.refs[t[i]] == 1)]
+        order += [i for i in range(hi - 1, lo - 1, -1) if t[i] >= 0 and i not in order]
+        for i in order:
+            self.let_go(t[i])
+            t[i] = -1
+
+    def append(self, s, n):
+        have, need = self.nblk(self.lens[s]), self.nblk(self.lens[s] + n)
+        if need > self.mb:
+            return "unsupported"
+        if need - have > len(self.free) + len(self.lru):
+            return "out"
+        for i in range(have, need):
+            self.tab[s][i] = self.pop()
+        self.lens[s] += n
+        return "ok"
+
+    def rollback(self, s, n):
+        L2 = self.lens[s] - n
+        if n < 0 or L2 < 0 or (self.kept[s] > 0 and L2 - self.w + 1 < self.kept[s] * self.bs):
+            return "bad"
+        if L2 % self.bs and n > 0:
+            b = self.tab[s][L2 // self.bs]
+            if b >= 0 and self.refs[b] > 1:
+                return "bad"
+        self.release_range(s, self.nblk(L2), self.nblk(self.lens[s]))
+        self.lens[s] = L2
+        return "ok"
+
+    def drop(self, s):
+        self.release_range(s, self.kept[s], self.nblk(self.lens[s]))
+        self.lens[s], self.kept[s] = 0, 0
+
+    def evict(self, s, oldest):
+        if self.w <= 0 or oldest - self.w + 1 <= 0:
+            return []
+        upto = min((oldest - self.w + 1) // self.bs, self.nblk(self.lens[s]))
+        out = []
+        for i in range(self.kept[s], upto):
+            if self.tab[s][i] >= 0:
+                out.append(self.tab[s][i])
+                self.let_go(self.tab[s][i])
+                self.tab[s][i] = -1
+        self.kept[s] = max(self.kept[s], upto)
+        return out
+
+    def publish(self, s, keys):
+        t = self.tab[s]
+        if len(keys) * self.bs > self.lens[s] or any(t[i] < 0 for i in range(len(keys))):
+            return "bad"
+        for i, k in enumerate(keys):
+            if t[i] in self.key_of or k in self.registry:
+                continue
+            self.registry[k], self.key_of[t[i]] = t[i], k
+        return "ok"
+
+    def attach(self, s, keys):
+        if self.lens[s] or self.kept[s]:
+            return -1
+        k = 0
+        while k < len(keys) and k < self.mb and keys[k] in self.registry:
+            b = self.registry[keys[k]]
+            if self.refs[b] == 0:
+                self.lru.remove(b)
+                self.revived += 1
+            self.refs[b] += 1
+            self.tab[s][k] = b
+            k += 1
+        self.lens[s] = k * self.bs
+        return k
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_operations_with_prefix_caching_match_the_model(seed):
+    """Random appends, rollbacks, releases, preemptions, evictions, publishes and
+    prefix attaches, against the model; prompts are drawn from a few shared
+    ones, so keys repeat across sequences and cached blocks are revived and
+    reclaimed."""
+    rng = np.random.default_rng(100 + seed)
+    nb, bs, ns, mb, w = 24, int(rng.choice([4, 16])), 5, 10, int(rng.choice([0, 23]))
+    bm = BlockManager(nb, bs, ns, mb, w)
+    m = PrefixModel(nb, bs, ns, mb, w)
+    prompt = [0] * ns   # which shared prompt each sequence's keys come from
+
+    def keys_of(p, n):
+        return np.array([1000 * (p + 1) + i for i in range(n)], np.uint64)
+
+    for _ in range(600):
+        s = int(rng.integers(ns))
+        op = rng.choice(["append", "append", "rollback", "release", "preempt", "evict",
+                         "publish", "attach", "attach"])
+        if op == "append":
+            n = int(rng.integers(0, 20))
+            want = m.append(s, n)
+            try:
+                slots = bm.append(s, n)
+                got = "ok"
+                L = m.lens[s]
+                exp = [m.tab[s][p // bs] * bs + p % bs for p in range(L - n, L)]
+                assert slots.tolist() == exp
+            except pa.PaError as e:
+                got = {pa.PA_ERR_OUT_OF_BLOCKS: "out", pa.PA_ERR_UNSUPPORTED: "unsupported"}[
+                    e.status]
+            assert got == want
+        elif op == "rollback":
+            n = int(rng.integers(0, 12))
+            want = m.rollback(s, n)
+            try:
+                bm.rollback(s, n)
+                got = "ok"
+            except pa.PaError:
+                got = "bad"
+            assert got == want
+        elif op in ("release", "preempt"):
+            m.drop(s)
+            getattr(bm, op)(s)
+        elif op == "evict":
+            oldest = m.lens[s]
+            want = m.evict(s, oldest)
+            assert bm.evict_window(s, oldest).tolist() == want
+        elif op == "publish":
+            n = int(rng.integers(0, m.lens[s] // bs + 2))
+            keys = keys_of(prompt[s], n)
+            want = m.publish(s, keys.tolist())
+            try:
+                bm.publish(s, keys)
+                got = "ok"
+            except pa.PaError:
+                got = "bad"
+            assert got == want
+        else:
+            p = int(rng.integers(3))
+            keys = keys_of(p, int(rng.integers(1, mb + 1)))
+            want = m.attach(s, keys.tolist())
+            try:
+                got = bm.attach_prefix(s, keys)
+            except pa.PaError:
+                got = -1
+            assert got == want
+            if want >= 0:
+                prompt[s] = p
+        tab, lens = check_invariants(bm, ns, shared_ok=True)
+        assert lens.tolist() == m.lens and tab.tolist() == m.tab
+        st = bm.stats()
+        assert st["cached_blocks"] == len(m.lru) and st["free_blocks"] == len(m.free)
+        assert st["reclaimed_blocks"] == m.reclaimed and st["revived_blocks"] == m.revived

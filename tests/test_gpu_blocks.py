@@ -159,3 +159,60 @@ def test_shared_prefix_blocks(dtype, olib):
     torch.cuda.synchronize()
     assert int(err[0].item()) == 0
     assert_close(outc.double().cpu().numpy(), refc, "chunk over shared blocks")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "i8-bf16"])
+def test_revived_prefix_blocks_after_the_request_ended(dtype, olib):
+    """"llminfer", Prefix KV cache reuse: r1 writes and publishes its prompt,
+    decodes and finishes; an unrelated request then needs more blocks than are
+    free, so the cache gives back r1's last prompt block (least recently used);
+    r2 with r1's prompt attaches the first five blocks from the cache and
+    appends its own tokens.  Decode of both live requests matches the oracle."""
+    cache_dt, q_dt = (dtype.split("-") + [None])[:2]
+    q_dt = q_dt or cache_dt
+    src = "bf16"
+    nb = 18
+    bm = BlockManager(nb, BS, max_seqs=3, max_blocks_per_seq=16)
+    cache = pa.PagedCache(nb, HKV, D, cache_dt)
+    cache_o = oracle.Cache(cache_dt, nb, HKV, D)
+    oracle_poison(cache_o, cache_dt)
+    if cache_dt == "i8":
+        cache.k.fill_(POISON_CODE), cache.v.fill_(POISON_CODE)
+        cache.k_scale.fill_(float("nan")), cache.v_scale.fill_(float("nan"))
+    else:
+        cache.k.fill_(float("nan")), cache.v.fill_(float("nan"))
+
+    def add(seq, n, stream):
+        slots = bm.append(seq, n)
+        _write(cache, cache_o, I.normal_bits((n, HKV, D), src, 6, stream),
+               I.normal_bits((n, HKV, D), src, 6, stream + 1), slots, src, olib)
+
+    add(0, 100, 10)                               # r1's prompt: 6 full blocks + 4
+    keys = np.arange(500, 506, dtype=np.uint64)
+    bm.publish(0, keys)
+    add(0, 1, 12)                                 # r1 decodes a token, then ends
+    r1_table, _ = bm.tables(np.array([0], np.int32))
+    bm.release(0)
+    st = bm.stats()
+    assert st["cached_blocks"] == 6 and st["free_blocks"] == nb - 6
+    add(1, 16 * (nb - 6 + 1), 20)                 # all free blocks and one cached one
+    assert bm.stats()["reclaimed_blocks"] == 1
+    assert bm.attach_prefix(2, keys) == 5         # the prompt's last block was reclaimed
+    add(2, 20, 30)                                # r2 recomputes the rest of its prompt
+    add(1, 1, 40)
+    add(2, 1, 42)
+    tables, ctx = bm.tables(np.array([1, 2], np.int32))
+    assert (tables[1, :5] == r1_table[0, :5]).all()
+    sm = 1.0 / np.sqrt(D)
+    Hq = HKV * G
+    q = I.normal_bits((2, Hq, D), q_dt, 6, 4444)
+    ref = oracle.attention(cache_o, q, q_dt, np.arange(3, dtype=np.int32), tables, ctx,
+                           sm_scale=sm, window=0, lib=olib)
+    out = torch.empty((2, Hq, D), dtype=TORCH_DT[q_dt], device="cuda")
+    nbytes = pa.pa_decode_workspace_bytes(2, Hq, HKV, D, tables.shape[1], 0)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+    err = new_err()
+    pa.pa_decode(cache, out, bits_to_torch(q, q_dt), i32(tables), i32(ctx), sm, 0, ws, err)
+    torch.cuda.synchronize()
+    assert int(err[0].item()) == 0
+    assert_close(out.double().cpu().numpy(), ref, "decode over revived prefix blocks")

@@ -13,10 +13,12 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_240_gb300 as pa
 from paged_kv_cache_240_gb300 import _build
 from paged_kv_cache_240_gb300 import inputs as I
-from gpu_util import ATOL, RTOL, bits_to_torch, device_history, i32, new_err
+from gpu_util import (ATOL, RTOL, assert_close, bits_to_torch, device_history, i32, new_err,
+                      oracle_poison)
 
 pytestmark = pytest.mark.gpu
 
@@ -25,10 +27,14 @@ pytestmark = pytest.mark.gpu
     ("mha-7b", dict(num_seqs=6, lens=("uniform", 1500, 4096))),
     ("int8-kv", dict(num_seqs=5, lens=("uniform", 700, 3000))),
 ])
-def test_noalloc_matches_pa_decode_twice(name, kw):
+def test_noalloc_matches_pa_decode_twice(name, kw, olib):
     _build.build()
     w = I.make_workload(name, seed=17, **kw)
-    cache, err = device_history(w)
+    kh, vh = I.history_rows(w)
+    cache, err = device_history(w, kh, vh)
+    cache_o = oracle.Cache(w.cache_dtype, w.num_blocks, w.num_kv_heads, w.head_dim)
+    oracle_poison(cache_o, w.cache_dtype)
+    oracle.write_kv(cache_o, kh, vh, I.source_dtype(w), w.history_slot_mapping(), lib=olib)
     B = w.num_decode
     need = pa.pa_decode_workspace_bytes(B, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                         w.max_blocks_per_seq, w.window)
@@ -37,8 +43,8 @@ def test_noalloc_matches_pa_decode_twice(name, kw):
     tables, lens = i32(w.block_tables), i32(w.context_lens)
     sm = 1.0 / np.sqrt(w.head_dim)
     for call in range(2):  # the second call finds the first call's partials in the scratch
-        q = bits_to_torch(I.normal_bits((B, w.num_q_heads, w.head_dim), w.q_dtype, 40 + call, 7),
-                          w.q_dtype)
+        q_bits = I.normal_bits((B, w.num_q_heads, w.head_dim), w.q_dtype, 40 + call, 7)
+        q = bits_to_torch(q_bits, w.q_dtype)
         ref, got = torch.empty_like(q), torch.full_like(q, float("nan"))
         e1, e2 = new_err(), new_err()
         pa.pa_decode(cache, ref, q, tables, lens, sm, w.window, ws, e1)
@@ -48,6 +54,10 @@ def test_noalloc_matches_pa_decode_twice(name, kw):
         r, g = ref.double().cpu().numpy(), got.double().cpu().numpy()
         assert np.isfinite(g).all()
         assert (np.abs(g - r) <= ATOL + RTOL * np.abs(r)).all(), (name, call)
+        ref = oracle.attention(cache_o, q_bits, w.q_dtype, np.arange(B + 1, dtype=np.int32),
+                               w.block_tables, w.context_lens, sm_scale=sm, window=w.window,
+                               lib=olib)
+        assert_close(g, ref, "%s call %d vs the oracle" % (name, call))
 
 
 def test_noalloc_rejects_batches_beyond_its_scratch():
