@@ -534,16 +534,20 @@ def cpu_baseline_all_cores(w, budget_s, seed=0, num_seqs=None, procs=None):
 
 # Four 7B-shaped decoder layers' projections (n output channels, k inputs):
 # q, k, v, o 4096x4096, gate and up 11008x4096, down 4096x11008 -- 810 MB of int8
-# codes, over six times the L2, so every step streams the weights from HBM.
+# codes, over six times the L2, so every step streams the weights from HBM.  The
+# projections that read the same activations run as one grouped launch: (q, k,
+# v), (o), (gate, up), (down) -- four launches per layer.
 LINEAR_LAYERS = 4
-LINEAR_SHAPES = [(4096, 4096)] * 4 + [(11008, 4096)] * 2 + [(4096, 11008)]
+LINEAR_GROUPS = [[(4096, 4096)] * 3, [(4096, 4096)], [(11008, 4096)] * 2, [(4096, 11008)]]
+LINEAR_SHAPES = [shape for grp in LINEAR_GROUPS for shape in grp]
 LINEAR_METRIC = "weight-only INT8 linear: weight-read GB/s (% of GB300 HBM peak)"
 
 
-def linear_bytes(m, shapes):
-    """Algorithmic bytes of one pass: every code and scale once, the activations
-    in and the outputs out (16-bit)."""
-    return sum(n * k + 4 * n + 2 * m * k + 2 * m * n for n, k in shapes)
+def linear_bytes(m, groups):
+    """Algorithmic bytes of one pass: every code and scale once, each group's
+    activations in once and every output out (16-bit)."""
+    return sum(sum(n * k + 4 * n + 2 * m * n for n, k in grp) + 2 * m * grp[0][1]
+               for grp in groups)
 
 
 class OracleLinearSample:
@@ -558,7 +562,7 @@ class OracleLinearSample:
         self.codes = rng.integers(-127, 128, size=(n, k), dtype=np.int8)
         self.scales = (rng.random(n, dtype=np.float32) * 0.01 + 0.001).astype(np.float32)
         self.x = I.normal_bits((m, k), "bf16", 7, 1)
-        self.bytes = linear_bytes(m, [(n, k)])
+        self.bytes = linear_bytes(m, [[(n, k)]])
 
     def run(self):
         t0 = time.perf_counter()
@@ -566,19 +570,24 @@ class OracleLinearSample:
         return self.bytes, time.perf_counter() - t0
 
 
-def linear_layers(torch, shapes, m, seed, dev="cuda"):
-    """(codes, scales, x, y) of each projection in ``shapes``, drawn in order from
-    one seeded generator on ``dev``: codes uniform in [-127, 127], scales uniform
-    in [0.001, 0.011], m activation rows ~N(0, 1) in bf16, y the bf16 output."""
+def linear_layers(torch, groups, m, seed, dev="cuda"):
+    """Per group (x, [(codes, scales, y)]), drawn in order from one seeded
+    generator on ``dev``: codes uniform in [-127, 127], scales uniform in
+    [0.001, 0.011], m activation rows ~N(0, 1) in bf16 shared by the group, y the
+    bf16 outputs."""
     gen = torch.Generator(device=dev).manual_seed(seed)
-    mats = []
-    for n, k in shapes:
-        codes = torch.randint(-127, 128, (n, k), dtype=torch.int8, device=dev, generator=gen)
-        scales = torch.rand(n, device=dev, generator=gen) * 0.01 + 0.001
+    out = []
+    for grp in groups:
+        k = grp[0][1]
         x = torch.randn((m, k), device=dev, generator=gen).to(torch.bfloat16)
-        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-        mats.append((codes, scales, x, y))
-    return mats
+        mats = []
+        for n, _ in grp:
+            codes = torch.randint(-127, 128, (n, k), dtype=torch.int8, device=dev, generator=gen)
+            scales = torch.rand(n, device=dev, generator=gen) * 0.01 + 0.001
+            y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+            mats.append((codes, scales, y))
+        out.append((x, mats))
+    return out
 
 
 def bench_linear(args):
@@ -586,10 +595,11 @@ def bench_linear(args):
     world = int(os.environ.get("WORLD_SIZE", 1))
     m = args.num_seqs or 8
     layers = args.layers or LINEAR_LAYERS
-    shapes = LINEAR_SHAPES * layers
-    step_bytes = linear_bytes(m, shapes)
+    groups = LINEAR_GROUPS * layers
+    step_bytes = linear_bytes(m, groups)
     cfg = {"workload": "int8-linear", "tokens": m, "layers": layers,
-           "shapes_n_k": LINEAR_SHAPES, "weight_bytes": sum(n * k for n, k in shapes),
+           "groups_n_k": LINEAR_GROUPS,
+           "weight_bytes": sum(n * k for grp in groups for n, k in grp),
            "activation_dtype": "bf16", "l2": "inputs larger than L2"}
     from paged_kv_cache_240_gb300 import inputs as I
     if args.impl == "reference":
@@ -598,18 +608,18 @@ def bench_linear(args):
         import oracle
         oracle.build()
         smp = OracleLinearSample(m, I)
-        rates = []
+        nbytes, secs = 0, 0.0
         for i in range(args.warmup + args.steps):
             b, dt = smp.run()
             if i >= args.warmup:
-                rates.append(b / dt)
-        value = statistics.median(rates) / 1e9
+                nbytes, secs = nbytes + b, secs + dt
+        value = nbytes / secs / 1e9
         print(json.dumps({
             "impl": "reference", "metric": LINEAR_METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": step_bytes / (value * 1e9) * 1e3, "higher_is_better": True,
+            "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": cfg,
+            "config": dict(cfg, sample_bytes_per_step=nbytes / args.steps),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": "per step: one 4096x4096 layer, %d tokens" % m},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -622,15 +632,14 @@ def bench_linear(args):
     from __graft_entry__ import build
     build()
     from paged_kv_cache_240_gb300 import linear as L
-    mats = linear_layers(torch, shapes, m, args.seed + 1000 * rank)
-    nbytes = max(L.int8_workspace_bytes(m, n, k) for n, k in shapes)
-    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
-    launches = sum(1 + (1 if L.int8_workspace_bytes(m, n, k) else 0) for n, k in shapes)
+    layers_dev = linear_layers(torch, groups, m, args.seed + 1000 * rank)
+    launches = len(groups)  # one grouped launch per group, splits merged in the launch
     stream = torch.cuda.Stream()
 
     def step():
-        for codes, scales, x, y in mats:
-            L.int8_linear(codes, scales, x, out=y, workspace=ws)
+        for x, mats in layers_dev:
+            L.int8_linear_grouped([(c, sc, None) for c, sc, _ in mats], x,
+                                  outs=[y for _, _, y in mats])
 
     run = capture(torch, step, stream).replay if not args.no_graph else step
     try:
@@ -651,9 +660,10 @@ def bench_linear(args):
         if world > 1:
             torch.distributed.barrier()
         clk = clocks.stop()
-        # end to end: every layer's activations in from pinned memory, outputs back
-        hx = [x.cpu().pin_memory() for _, _, x, _ in mats]
-        hy = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _, _, _, y in mats]
+        # end to end: every group's activations in from pinned memory, outputs back
+        hx = [x.cpu().pin_memory() for x, _ in layers_dev]
+        ys = [y for _, mats in layers_dev for _, _, y in mats]
+        hy = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys]
         h2d = sum(t.numel() * t.element_size() for t in hx)
         d2h = sum(t.numel() * t.element_size() for t in hy)
         e2e_steps = max(3, min(args.steps, 100))
@@ -661,10 +671,10 @@ def bench_linear(args):
         torch.cuda.synchronize()
         s0.record(stream)
         for _ in range(e2e_steps):
-            for (_, _, x, _), t in zip(mats, hx):
+            for (x, _), t in zip(layers_dev, hx):
                 x.copy_(t, non_blocking=True)
             run()
-            for (_, _, _, y), t in zip(mats, hy):
+            for y, t in zip(ys, hy):
                 t.copy_(y, non_blocking=True)
         s1.record(stream)
         torch.cuda.synchronize()
@@ -688,7 +698,8 @@ def bench_linear(args):
                          # the record is of the default stack (four layers, 8 tokens)
                          "traffic": (recorded_traffic("int8-linear", "linear")
                                      if (layers, m) == (LINEAR_LAYERS, 8) else None),
-                         "kernel": "pa_linear_int8 (int8 codes -> exact f16, mma.sync m16n8k16)",
+                         "kernel": "pa_linear_int8_grouped (int8 codes -> exact f16, mma.sync "
+                                   "m16n8k16; k splits merged over distributed shared memory)",
                          "peak_source": src + " hbm_gbs",
                          "frac_of_nominal": achieved / NOMINAL["GB/s"]},
             "p10_p50_p90_step_ms": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)]}

@@ -132,10 +132,12 @@ pa_status pa_write_kv(const pa_cache *cache, const void *k, const void *v, pa_dt
  *   workspace     device scratch for split-K partials, at least
  *                 pa_decode_workspace_bytes(...) bytes (may be NULL if that is 0)
  *
- * The context is cut into partitions of whole blocks; each partition's online-
- * softmax state (max, normaliser, unnormalised output) goes to the workspace and
- * a second kernel merges them.  The partition size is chosen from the batch shape
- * and the device's SM count; the result does not depend on it beyond rounding.
+ * Long contexts are cut into partitions of whole blocks, each with its own
+ * online-softmax state (max, normaliser, unnormalised output); the states go to
+ * the workspace and a second kernel merges them.  The partition size (64 blocks,
+ * halved while the batch leaves SMs without two CTAs each) is chosen from the
+ * batch shape and the device's SM count; the result does not depend on it
+ * beyond rounding.  pa_decode_partitioned can instead merge inside the launch.
  */
 pa_status pa_decode(const pa_cache *cache, void *out, const void *q, pa_dtype q_dtype,
                     int num_seqs, int num_q_heads, const int32_t *block_tables,
@@ -144,9 +146,16 @@ pa_status pa_decode(const pa_cache *cache, void *out, const void *q, pa_dtype q_
                     void *stream);
 
 /*
- * pa_decode_partitioned -- pa_decode with an explicit partition size in blocks
- * (partition_blocks >= 1), or 0 for the automatic choice.  A partition size at
- * least as large as the longest context gives a single pass with no merge.
+ * pa_decode_partitioned -- pa_decode with an explicit partitioning:
+ *   partition_blocks >= 1   partitions of that many blocks, merged through the
+ *                           workspace (a size at least as large as the longest
+ *                           context gives a single pass with no merge);
+ *   partition_blocks <= -1  each sequence's visible blocks split evenly into
+ *                           -partition_blocks partitions (at most 16, fewer when
+ *                           the sequence has fewer blocks), merged in the launch
+ *                           by a thread-block cluster (falls back to the
+ *                           workspace merge if the device cannot hold it);
+ *   0                       the automatic choice of pa_decode.
  */
 pa_status pa_decode_partitioned(const pa_cache *cache, void *out, const void *q,
                                 pa_dtype q_dtype, int num_seqs, int num_q_heads,
@@ -157,8 +166,9 @@ pa_status pa_decode_partitioned(const pa_cache *cache, void *out, const void *q,
 
 /*
  * Workspace bytes pa_decode / pa_decode_partitioned need for these arguments
- * (partition_blocks 0 = the automatic choice, evaluated on the current device).
- * Returns 0 when no workspace is needed, (size_t)-1 on bad arguments.
+ * (partition_blocks as for pa_decode_partitioned; 0 = the automatic choice,
+ * evaluated on the current device).  Returns 0 when no workspace is needed (a
+ * single pass, or a merge inside the launch), (size_t)-1 on bad arguments.
  */
 size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                                  int head_dim, int max_blocks_per_seq, int window,
@@ -171,10 +181,11 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads
  * engine that owns all allocation, or a serving loop that must never call
  * cudaMalloc/cudaFree because those calls can synchronise the whole device.
  *
- * Same arguments and result as pa_decode, without workspace: the split-K
- * partials live in a scratch array of PA_NOALLOC_SCRATCH_BYTES compiled into the
- * library, which every device that loads the library holds until the process
- * exits.  The call allocates nothing.
+ * Same arguments and result as pa_decode, without workspace: when the batch
+ * takes pa_decode's workspace merge (very few (sequence, kv head) pairs), the
+ * split-K partials live in a scratch array of PA_NOALLOC_SCRATCH_BYTES compiled
+ * into the library, which every device that loads the library holds until the
+ * process exits; other batches need no scratch.  The call allocates nothing.
  *   - Returns PA_ERR_UNSUPPORTED, launching nothing, when this batch's partials
  *     would exceed PA_NOALLOC_SCRATCH_BYTES (pa_decode_workspace_bytes with
  *     partition_blocks = 0 gives the size); use pa_decode for such batches.

@@ -44,9 +44,12 @@ pa_status pa_linear_int8_quantize(const void *w, pa_dtype w_dtype, int n, int k,
                                   float *scales, void *stream);
 
 /*
- * Workspace for pa_linear_int8 (bytes): partial sums when the call splits the k
- * range across thread blocks to fill the GPU.  A smaller workspace (even none)
- * is accepted; the call then splits less.
+ * Workspace for pa_linear_int8 (bytes).  When the output channels are too few
+ * to fill the GPU, the call splits the k range across thread blocks; up to 8
+ * splits add their partial sums inside the launch (a thread-block cluster, no
+ * workspace), more -- only for very few channels over a long k -- go through
+ * this workspace and a second kernel.  A smaller workspace (even none) is
+ * accepted; the call then splits less.
  */
 size_t pa_linear_int8_workspace_bytes(int m, int n, int k);
 
@@ -54,6 +57,24 @@ size_t pa_linear_int8_workspace_bytes(int m, int n, int k);
 pa_status pa_linear_int8(const int8_t *codes, const float *scales, const void *bias, const void *x,
                          pa_dtype x_dtype, int m, int n, int k, void *y, void *workspace,
                          size_t workspace_bytes, void *stream);
+
+/*
+ * pa_linear_int8_grouped -- count (1..4) weight-only INT8 linears that read the
+ * same activations x [m][k], in one launch: y[i] = x * dequant(codes[i],
+ * scales[i])^T (+ bias[i]), y[i] [m][n[i]].  A decoder layer's q, k and v
+ * projections, or its gate and up projections, share x ("PyTorch LLM Serving
+ * Engine", "What is implemented": the fused INT8 backend serves every
+ * projection).  codes, scales, bias (NULL, or an array whose entries may be
+ * NULL), n and y are HOST arrays of count entries; the pointers in them are
+ * device pointers with the alignment and type rules of pa_linear_int8, every
+ * n[i] a multiple of 16.  Each matrix's result is pa_linear_int8's on it alone
+ * up to the order of the fp32 additions: the k range may be split differently
+ * (at most 8 splits, merged in the launch; no workspace).
+ */
+pa_status pa_linear_int8_grouped(int count, const int8_t *const *codes,
+                                 const float *const *scales, const void *const *bias,
+                                 const int *n, const void *x, pa_dtype x_dtype, int m, int k,
+                                 void *const *y, void *stream);
 
 #ifdef __cplusplus
 }

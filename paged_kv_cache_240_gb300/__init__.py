@@ -38,7 +38,7 @@ EXPORTED_SYMBOLS = ("pa_write_kv", "pa_decode", "pa_decode_partitioned",
                     "pa_blocks_evict_window", "pa_blocks_tables", "pa_blocks_context_len",
                     "pa_blocks_get_stats", "pa_blocks_publish", "pa_blocks_attach_prefix",
                     "pa_linear_int8_quantize", "pa_linear_int8_workspace_bytes",
-                    "pa_linear_int8", "pa_selftest_bounded_wait")
+                    "pa_linear_int8", "pa_linear_int8_grouped", "pa_selftest_bounded_wait")
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 

@@ -53,7 +53,13 @@ struct AttnParams {
   int part_blocks, num_parts;        // decode: blocks per partition, partitions per (seq, head)
   int num_q_tokens, max_q_len, q_tiles;  // prefill
   float scale_log2;                  // sm_scale * log2(e)
+  // decode: how partitions are formed and merged (kMergeWorkspace: fixed
+  // part_blocks per partition, partials merged by a second kernel;
+  // kMergeCluster: each sequence's blocks split evenly into at most num_parts
+  // partitions of at least min_part_blocks, merged inside the launch)
+  int merge_mode, min_part_blocks;
 };
+constexpr int kMergeWorkspace = 0, kMergeCluster = 1;
 
 // Shared-memory layout of one CTA (from a base aligned to the swizzle atom):
 // stages, int8 scales, barriers and per-stage flags.  After the pipeline drains,

@@ -7,10 +7,22 @@
 // partition of whole blocks).  Its four consumer warps take the partition's
 // blocks round-robin, each keeping its own online-softmax state for the same
 // heads; the states are merged in shared memory at the end.  A sequence whose
-// visible context fits in one partition writes its output directly; otherwise
-// each partition writes (max, normaliser, unnormalised output) to the workspace
-// and pa_reduce_kernel merges them:  M = max_p m_p,
-//   out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p   (log2-domain maxima).
+// visible context fits in one partition writes its output directly.  Longer
+// ones are split, and the partitions' states (max, normaliser, unnormalised
+// output) are merged as  M = max_p m_p,
+//   out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p   (log2-domain maxima),
+// in one of two ways:
+//   - cluster merge: the num_parts CTAs of a (sequence, kv head, row group) form
+//     one thread-block cluster; each sequence's visible blocks are split evenly
+//     into as many partitions as its length warrants (up to num_parts, each of
+//     at least min_part_blocks), every CTA leaves its state in its own shared
+//     memory, and after a cluster barrier the CTAs merge the output elements
+//     between them, reading the others' states over distributed shared memory.
+//     One launch, no workspace.
+//   - workspace merge: partitions of a fixed part_blocks write their states to
+//     a caller-provided workspace and pa_reduce_kernel merges them; used when
+//     the batch has too few (sequence, kv head) units for clusters of at most 16
+//     CTAs to fill the GPU, or when the caller fixes the partition size.
 // Partition boundaries and the merge order depend only on logical positions, so
 // the result is bit-identical under any relabelling of physical blocks.
 #include <algorithm>
@@ -286,13 +298,21 @@ __device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2]
   }
 }
 
-// Number of partitions sequence `seq` needs; also gives its visible range.
+// Partitions of a sequence with visible context L, their size in blocks (psz)
+// and the visible range (keys from lo, blocks first..last).  L >= 1.
 __device__ __forceinline__ int decode_parts(const AttnParams& p, int L, int& lo, int& first,
-                                            int& last) {
+                                            int& last, int& psz) {
   lo = p.window > 0 ? max(0, L - p.window) : 0;
   first = lo / kBlock;
   last = (L - 1) / kBlock;
-  return (last - first + p.part_blocks) / p.part_blocks;
+  const int nb = last - first + 1;
+  if (p.merge_mode == kMergeCluster) {
+    const int np = max(1, min(p.num_parts, (nb + p.min_part_blocks - 1) / p.min_part_blocks));
+    psz = (nb + np - 1) / np;
+  } else {
+    psz = p.part_blocks;
+  }
+  return (nb + psz - 1) / psz;
 }
 
 // Decode CTAs have no producer warp: warp w of the four owns blocks w, w+4,
@@ -308,8 +328,38 @@ template <int MODE, int D>
 struct DecSmem {
   static constexpr int kOS = D + 4;  // fp32 row stride of the warp-merge area
   static constexpr int kMergeBytes = kDecWarps * kDecHeads * (kOS + 2) * 4;
-  static_assert(kMergeBytes <= Smem<MODE, D>::kDataBytes, "merge area must fit the stages");
+  // after the warp merge, this CTA's partition state for the cluster merge:
+  // m[8], l[8], ok, then o[8][D] (fp32)
+  static constexpr int kPartOff = (kMergeBytes + 127) / 128 * 128;
+  static constexpr int kPartOOff = kPartOff + (2 * kDecHeads + 4) * 4;
+  static constexpr int kPartBytes = kPartOOff - kPartOff + kDecHeads * D * 4;
+  static_assert(kPartOff + kPartBytes <= Smem<MODE, D>::kDataBytes,
+                "merge areas must fit the stages");
 };
+
+// Cluster-wide barrier: every thread of every CTA in the cluster arrives, and
+// this CTA's earlier shared-memory writes are visible to the others after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// fp32 at the same shared-memory offset as `local` in cluster CTA `rank`.
+__device__ __forceinline__ float ld_cluster_f32(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)),
+               "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
 
 // Warp-level copy of one block of kv head kvh into stage `slot`: lane 0 arms
 // the stage's barrier and issues the TMA boxes; for int8, lanes 0-7 fetch the
@@ -356,6 +406,8 @@ __global__ void __launch_bounds__(kDecThreads, MODE == kI8 ? 5 : 3)
     pa_decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_wait();               // the kernel before (say, the K/V write) is complete
+  pdl_launch_dependents();  // the split-K merge may start its launch
   const int b = blockIdx.y;
   const int part = blockIdx.x % p.num_parts;
   const int hx = blockIdx.x / p.num_parts;
@@ -372,11 +424,15 @@ __global__ void __launch_bounds__(kDecThreads, MODE == kI8 ? 5 : 3)
         out[((long long)b * p.num_q_heads + h0 + idx / D) * D + idx % D] = to_out<QT>(0.0f);
     return;
   }
-  int lo, first, last;
-  const int nparts = decode_parts(p, L, lo, first, last);
-  if (part >= nparts) return;
-  const int blk0 = first + part * p.part_blocks;
-  const int nblk = min(p.part_blocks, last + 1 - blk0);
+  int lo, first, last, psz;
+  const int nparts = decode_parts(p, L, lo, first, last, psz);
+  // a split sequence of the cluster merge: every CTA of the cluster takes part in
+  // the merge, including those its length leaves without a partition; otherwise
+  // (the decision is the same for the whole cluster) such CTAs have nothing to do
+  const bool cluster_merge = p.merge_mode == kMergeCluster && nparts > 1;
+  if (part >= nparts && !cluster_merge) return;
+  const int blk0 = first + part * psz;
+  const int nblk = part < nparts ? min(psz, last + 1 - blk0) : 0;
   const int nmine = nblk > warp ? (nblk - warp + kDecWarps - 1) / kDecWarps : 0;  // this warp's blocks
 
   const SmemPtrs s = smem_ptrs<MODE, D>(smem);
@@ -474,7 +530,8 @@ __global__ void __launch_bounds__(kDecThreads, MODE == kI8 ? 5 : 3)
       for (int i = 0; i < 4; i++) o[mt][i] = (o[mt][i] - 1152.0f * lv[i & 1]) * f[i & 1];
   }
   __syncthreads();  // every stage consumed: reuse them for the merge
-  if (*s.abort_flag) return;
+  const bool aborted = *s.abort_flag != 0;
+  if (aborted && !cluster_merge) return;
 
   constexpr int OS = DecSmem<MODE, D>::kOS;
   float* mw = reinterpret_cast<float*>(s.stages);  // [warp][head]
@@ -494,6 +551,61 @@ __global__ void __launch_bounds__(kDecThreads, MODE == kI8 ? 5 : 3)
       if (h < rows) ow[(warp * kDecHeads + h) * OS + ot_col<MODE, D>(mt, g, i >> 1)] = o[mt][i];
     }
   __syncthreads();
+
+  if (cluster_merge) {
+    // this CTA's partition state, then the cluster merge of every output element
+    using DS = DecSmem<MODE, D>;
+    float* pm = reinterpret_cast<float*>(s.stages + DS::kPartOff);  // [head]
+    float* pl = pm + kDecHeads;                                      // [head]
+    int* pok = reinterpret_cast<int*>(pl + kDecHeads);
+    float* po = reinterpret_cast<float*>(s.stages + DS::kPartOOff);  // [head][D]
+    for (int idx = threadIdx.x; idx < rows * D; idx += kDecThreads) {
+      const int r = idx / D, d = idx % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; w++) M = fmaxf(M, mw[w * kDecHeads + r]);
+      float num = 0.0f, den = 0.0f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kDecWarps; w++) {
+          const float e = exp2f(mw[w * kDecHeads + r] - M);
+          num += e * ow[(w * kDecHeads + r) * OS + d];
+          den += e * lw[w * kDecHeads + r];
+        }
+      }
+      po[r * D + d] = num;
+      if (d == 0) {
+        pm[r] = M;
+        pl[r] = den;
+      }
+    }
+    // the cluster rank is the partition (grid x = partition + num_parts * ...)
+    if (threadIdx.x == 0) *pok = (!aborted && cluster_ctarank() == (uint32_t)part) ? 1 : 0;
+    cluster_sync_all();  // every partition's state is in place
+    bool all_ok = true;
+    for (int q = 0; q < nparts; q++)
+      all_ok = all_ok && __float_as_int(ld_cluster_f32(pok, q)) == 1;
+    if (all_ok) {
+      for (int idx = part * kDecThreads + threadIdx.x; idx < rows * D;
+           idx += p.num_parts * kDecThreads) {
+        const int r = idx / D, d = idx % D;
+        float M = -INFINITY;
+        for (int q = 0; q < nparts; q++) M = fmaxf(M, ld_cluster_f32(pm + r, q));
+        float num = 0.0f, den = 0.0f;
+        if (M != -INFINITY) {
+          for (int q = 0; q < nparts; q++) {
+            const float e = exp2f(ld_cluster_f32(pm + r, q) - M);
+            num += e * ld_cluster_f32(po + r * D + d, q);
+            den += e * ld_cluster_f32(pl + r, q);
+          }
+        }
+        out[((long long)b * p.num_q_heads + h0 + r) * D + d] =
+            to_out<QT>(den > 0.0f ? num / den : 0.0f);
+      }
+    }
+    cluster_sync_all();  // no CTA leaves while another still reads its state
+    return;
+  }
 
   const bool direct = nparts == 1;
   for (int idx = threadIdx.x; idx < rows * D; idx += kDecThreads) {
@@ -533,6 +645,8 @@ constexpr int kRedThreads = 128;
 
 template <int D, typename QT>
 __global__ void __launch_bounds__(kRedThreads) pa_reduce_kernel(const AttnParams p) {
+  pdl_wait();  // the partitions' states are written
+  pdl_launch_dependents();
   __shared__ float red[kRedThreads / 32];
   __shared__ float4 part_sum[kRedThreads / 32][D / 4];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -540,8 +654,8 @@ __global__ void __launch_bounds__(kRedThreads) pa_reduce_kernel(const AttnParams
   const int b = (int)(hrow / p.num_q_heads);
   const int L = clamp_context(p, b, false);
   if (L == 0) return;
-  int lo, first, last;
-  const int nparts = decode_parts(p, L, lo, first, last);
+  int lo, first, last, psz;
+  const int nparts = decode_parts(p, L, lo, first, last, psz);
   if (nparts <= 1) return;  // written directly by the attention kernel
   const long long base = hrow * p.num_parts;
 
@@ -618,30 +732,105 @@ int max_blocks_touched(int max_blocks_per_seq, int window) {
   return std::min(max_blocks_per_seq, (window + 2 * kBlock - 2) / kBlock);
 }
 
+// Cluster merge: at most 16 CTAs per cluster (the non-portable maximum, checked
+// on the device).
+constexpr int kMaxCluster = 16;
+
+// Whether a cluster of `size` decode CTAs with the largest shared-memory
+// footprint (16-bit cache, head_dim 128) can be resident on the current device;
+// asked of the occupancy calculator once per device and size.
+bool cluster_fits(int size) {
+  if (size <= 1) return true;
+  if (size > kMaxCluster) return false;
+  static std::mutex mu;
+  static signed char known[64][kMaxCluster + 1];  // 0 unknown, 1 fits, 2 does not
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (known[dev][size] == 0) {
+    auto kern = pa_decode_kernel<kF16, 128, __half>;
+    constexpr int smem = Smem<kF16, 128>::kBytes;
+    bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+                  cudaSuccess &&
+              (size <= 8 || cudaFuncSetAttribute(kern,
+                                                 cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                                 1) == cudaSuccess);
+    int n = 0;
+    if (ok) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)size, 1, 1);
+      cfg.blockDim = dim3(kDecThreads, 1, 1);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = (unsigned)size;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      ok = cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= 1;
+    }
+    cudaGetLastError();  // a refusal here only means "no"
+    known[dev][size] = ok ? 1 : 2;
+  }
+  return known[dev][size] == 1;
+}
+
 struct Split {
-  int part_blocks, num_parts;
+  int mode;             // kMergeWorkspace or kMergeCluster
+  int part_blocks;      // workspace: blocks per partition
+  int num_parts;        // partitions per (sequence, kv head, row group) at most
+  int min_part_blocks;  // cluster: smallest partition
 };
 
-// Partition size: 64 blocks (1024 tokens) unless the batch is too small to give
-// every SM two CTAs, in which case halve it (down to 4 blocks).
-Split choose_split(int num_seqs, int num_kv_heads, int row_groups, int max_blocks_per_seq,
-                   int window, int partition_blocks) {
-  const int maxb = max_blocks_touched(max_blocks_per_seq, window);
+// The workspace split: partitions of 64 blocks (1024 tokens) unless the batch is
+// too small to give every SM two CTAs, in which case halve them (down to 4).
+Split workspace_split(long long units, int maxb, int partition_blocks, int sms) {
   int pb = partition_blocks;
   if (pb <= 0) {
-    const long long units = (long long)num_seqs * num_kv_heads * row_groups;
-    long long target = 2LL * std::max(current_sm_count(), 1);
+    const long long target = 2LL * sms;
     pb = 64;
     while (pb > 4 && units * ((maxb + pb - 1) / pb) < target) pb /= 2;
   }
   Split s;
+  s.mode = kMergeWorkspace;
   s.part_blocks = std::max(1, std::min(pb, maxb));
   s.num_parts = (maxb + s.part_blocks - 1) / s.part_blocks;
+  s.min_part_blocks = 1;
+  return s;
+}
+
+// partition_blocks > 0: fixed partitions, workspace merge.  partition_blocks < 0:
+// each sequence split evenly into up to -partition_blocks partitions (at most 16),
+// cluster merge (a cluster the device cannot hold falls back to the workspace
+// merge).  0: the workspace merge with 64-block partitions, halved while the
+// batch gives the SMs fewer than two CTAs each.  Measured on GB300, the cluster
+// merge was never faster on the benchmark batches: evenly split clusters cost
+// every sequence P CTAs' fixed work (7B MHA, INT8 and mixed batches 1-18 %
+// slower), and on the Qwen2.5-1.5B batch, whose step is latency-bound, 16-CTA
+// clusters took 17.3 us against 16.9 us with the merge kernel.
+Split choose_split(int num_seqs, int num_kv_heads, int row_groups, int max_blocks_per_seq,
+                   int window, int partition_blocks) {
+  const int maxb = max_blocks_touched(max_blocks_per_seq, window);
+  const long long units = (long long)num_seqs * num_kv_heads * row_groups;
+  const int sms = std::max(current_sm_count(), 1);
+  if (partition_blocks > 0) return workspace_split(units, maxb, partition_blocks, sms);
+  if (partition_blocks == 0) return workspace_split(units, maxb, 0, sms);
+  int P = std::min(std::min(-partition_blocks, kMaxCluster), maxb);
+  const int min_part = 1;
+  P = std::max(P, 1);
+  if (!cluster_fits(P))
+    return workspace_split(units, maxb, partition_blocks < 0 ? (maxb + P - 1) / P : 0, sms);
+  Split s;
+  s.mode = kMergeCluster;
+  s.part_blocks = 0;
+  s.num_parts = P;
+  s.min_part_blocks = min_part;
   return s;
 }
 
 size_t workspace_for(int num_seqs, int num_q_heads, int head_dim, const Split& s) {
-  if (s.num_parts <= 1) return 0;
+  if (s.mode != kMergeWorkspace || s.num_parts <= 1) return 0;
   const size_t n = (size_t)num_seqs * num_q_heads * s.num_parts;
   return n * head_dim * 4 + 2 * n * 4 + 16;
 }
@@ -654,12 +843,19 @@ cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tmk, const CUt
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(p.num_parts * p.num_kv_heads * p.row_groups), (unsigned)num_seqs);
-  kern<<<grid, kDecThreads, smem, stream>>>(p, tmk, tmv);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || p.num_parts <= 1) return e;
+  // the partitions of a (sequence, kv head, row group) are one cluster when
+  // they merge in the launch
+  const bool cluster = p.merge_mode == kMergeCluster && p.num_parts > 1;
+  if (cluster && p.num_parts > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  e = pa_internal::launch_dependent(kern, grid, dim3(kDecThreads), smem, stream,
+                                    cluster ? (unsigned)p.num_parts : 1u, p, tmk, tmv);
+  if (e != cudaSuccess || cluster || p.num_parts <= 1) return e;
   const long long heads = (long long)num_seqs * p.num_q_heads;
-  pa_reduce_kernel<D, QT><<<(unsigned)heads, kRedThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return pa_internal::launch_dependent(pa_reduce_kernel<D, QT>, dim3((unsigned)heads),
+                                       dim3(kRedThreads), 0, stream, 1u, p);
 }
 
 template <int MODE, typename QT>
@@ -675,8 +871,7 @@ extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int n
                                             int head_dim, int max_blocks_per_seq, int window,
                                             int partition_blocks) {
   if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads ||
-      (head_dim != 64 && head_dim != 128) || max_blocks_per_seq < 1 || window < 0 ||
-      partition_blocks < 0)
+      (head_dim != 64 && head_dim != 128) || max_blocks_per_seq < 1 || window < 0)
     return (size_t)-1;
   const int G = num_q_heads / num_kv_heads;
   const int row_groups = (G + kDecHeads - 1) / kDecHeads;
@@ -696,7 +891,7 @@ extern "C" pa_status pa_decode_partitioned(const pa_cache* cache, void* out, con
   pa_status st = pa_internal::check_cache(cache);
   if (st != PA_OK) return st;
   if (num_seqs < 0 || num_q_heads < 1 || num_q_heads % cache->num_kv_heads ||
-      max_blocks_per_seq < 1 || window < 0 || partition_blocks < 0 || !err_flag ||
+      max_blocks_per_seq < 1 || window < 0 || !err_flag ||
       !(sm_scale == sm_scale) || sm_scale > 3.0e38f || sm_scale < -3.0e38f)
     return PA_ERR_INVALID_ARG;
   if (num_seqs == 0) return PA_OK;
@@ -741,6 +936,8 @@ extern "C" pa_status pa_decode_partitioned(const pa_cache* cache, void* out, con
   p.window = window;
   p.part_blocks = sp.part_blocks;
   p.num_parts = sp.num_parts;
+  p.merge_mode = sp.mode;
+  p.min_part_blocks = sp.min_part_blocks;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   if (need > 0) {
     const size_t n = (size_t)num_seqs * num_q_heads * sp.num_parts;

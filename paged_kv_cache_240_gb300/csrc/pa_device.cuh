@@ -186,6 +186,16 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
                : "r"(addr));
 }
 
+// D = A(16x32 s8, row) * B(32x8 s8, col) + D with int32 accumulation (exact).
+__device__ __forceinline__ void imma16832(int (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // Transpose of an 8x8 b16 matrix held one row pair per thread (the layout
 // ldmatrix and the MMA C fragment use): thread (g, t) gives row g, columns 2t,
 // 2t+1 and receives row g, columns 2t, 2t+1 of the transpose.
@@ -327,6 +337,22 @@ __device__ __forceinline__ int q_prescale_shift(float amax) {
 __device__ __forceinline__ float pow2i(int k) {  // 2^k for -126 <= k <= 127
   return __uint_as_float((uint32_t)(k + 127) << 23);
 }
+
+// ------------------------------------------------------------------ dependent launch
+//
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while the kernel before it in the
+// stream is still running, once every CTA of that kernel has signalled
+// (pdl_launch_dependents) or exited; it must pdl_wait() -- which returns when
+// the kernel before it has completed and its writes are visible -- before it
+// reads anything that kernel may have written.  Launched without the
+// attribute, pdl_wait returns at once.  The library's kernels signal at their
+// start and wait before their first read of an input, so only launch latency
+// and set-up overlap, never data.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ------------------------------------------------------------------ misc
 

@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(kThreads)
     pa_prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_wait();  // the kernel before (say, the K/V write) is complete
+  pdl_launch_dependents();
   const int n = blockIdx.y;
   const int tile = blockIdx.x % p.q_tiles;
   const int kvh = blockIdx.x / p.q_tiles;
@@ -167,8 +169,7 @@ cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap& tmk, const CU
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(p.q_tiles * p.num_kv_heads), (unsigned)num_seqs);
-  kern<<<grid, kThreads, smem, stream>>>(p, tmk, tmv);
-  return cudaGetLastError();
+  return pa_internal::launch_dependent(kern, grid, dim3(kThreads), smem, stream, 1u, p, tmk, tmv);
 }
 
 template <int MODE, typename QT>

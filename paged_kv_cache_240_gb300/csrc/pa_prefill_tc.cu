@@ -437,6 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   using LY = Layout<D>;
   constexpr bool BF = std::is_same<QT, __nv_bfloat16>::value;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  pdl_wait();  // the kernel before (say, the K/V write) is complete
+  pdl_launch_dependents();
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::kBarOff);
   uint64_t* k_full = bars;
@@ -1235,8 +1237,8 @@ cudaError_t launch_prefill_tc_ks(const AttnParams& p, const CUtensorMap& tmk,
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const unsigned grid = (unsigned)std::min<long long>(items, sms);
-  kern<<<grid, tc::kThreads, smem, stream>>>(pt, tmk, tmv, tmq, num_seqs, q_tma ? 1 : 0);
-  return cudaGetLastError();
+  return pa_internal::launch_dependent(kern, dim3(grid), dim3(tc::kThreads), smem, stream, 1u, pt,
+                                       tmk, tmv, tmq, num_seqs, q_tma ? 1 : 0);
 }
 
 // Chunks of at most 128 query rows (a few queries per sequence, e.g. a draft

@@ -42,6 +42,7 @@ constexpr int kWriteWarps = 8;
 // 16-bit cache: copy the row's bits.  D * 2 bytes per row = D/16 bytes per lane.
 template <int D>
 __global__ void __launch_bounds__(kWriteWarps * 32) write_copy_kernel(WriteParams p) {
+  pdl_launch_dependents();  // the attention call after it may start its launch now
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
   if (row >= (long long)p.num_tokens * p.num_kv_heads) return;
@@ -91,6 +92,7 @@ __device__ __forceinline__ void quantize_row(const float (&x)[E], int8_t (&q)[E]
 
 template <typename IT, int D>
 __global__ void __launch_bounds__(kWriteWarps * 32) write_quant_kernel(WriteParams p) {
+  pdl_launch_dependents();  // the attention call after it may start its launch now
   constexpr int E = D / 32;  // elements per lane
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);

@@ -18,6 +18,8 @@ def _lib():
         lib.pa_linear_int8_workspace_bytes.restype = S
         lib.pa_linear_int8.argtypes = [P, P, P, P, I, I, I, I, P, P, S, P]
         lib.pa_linear_int8.restype = I
+        lib.pa_linear_int8_grouped.argtypes = [I, P, P, P, P, P, I, I, I, P, P]
+        lib.pa_linear_int8_grouped.restype = I
         lib._pa_linear_ready = True
     return lib
 
@@ -55,3 +57,31 @@ def int8_linear(codes, scales, x, bias=None, out=None, workspace=None, stream=No
                                  _dtype_code(x), m, n, k, _ptr(out), _ptr(workspace), nbytes,
                                  _stream(stream)), "pa_linear_int8")
     return out
+
+
+def int8_linear_grouped(mats, x, outs=None, stream=None):
+    """One launch for up to four linears that read the same x [m, k]: mats is a
+    list of (codes [n_i, k], scales [n_i], bias [n_i] or None); returns the
+    outputs [m, n_i] in x's dtype (or fills ``outs``)."""
+    torch = _torch()
+    m, k = x.shape
+    count = len(mats)
+    if not 1 <= count <= 4:
+        raise PaError(1, "pa_linear_int8_grouped")
+    if outs is None:
+        outs = [torch.empty((m, c.shape[0]), dtype=x.dtype, device=x.device) for c, _, _ in mats]
+    for (codes, scales, bias), y in zip(mats, outs):
+        if codes.shape[1] != k or scales.shape[0] != codes.shape[0]:
+            raise PaError(1, "pa_linear_int8_grouped")
+        _check_cuda(codes, scales, bias, y)
+    _check_cuda(x)
+    vp = ctypes.c_void_p * count
+    arr_codes = vp(*[c.data_ptr() for c, _, _ in mats])
+    arr_scales = vp(*[s.data_ptr() for _, s, _ in mats])
+    arr_bias = vp(*[0 if b is None else b.data_ptr() for _, _, b in mats])
+    arr_y = vp(*[y.data_ptr() for y in outs])
+    arr_n = (ctypes.c_int * count)(*[int(c.shape[0]) for c, _, _ in mats])
+    _raise(_lib().pa_linear_int8_grouped(count, arr_codes, arr_scales, arr_bias, arr_n, _ptr(x),
+                                         _dtype_code(x), m, k, arr_y, _stream(stream)),
+           "pa_linear_int8_grouped")
+    return outs

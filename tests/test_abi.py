@@ -124,6 +124,24 @@ def test_linear_rejects_bad_arguments():
     assert lin(y=A + 1) == pa.PA_ERR_INVALID_ARG       # y not 2-byte aligned
     assert lin(scales=A + 2) == pa.PA_ERR_INVALID_ARG  # scales not 4-byte aligned
 
+    import ctypes as C
+    P4, N4 = C.c_void_p * 4, C.c_int * 4
+
+    def grp(count=2, codes=(A, A), scales=(A, A), n=(64, 32), x=A, y=(A, A), xdt=pa.PA_BF16,
+            m=8, k=256):
+        return lib.pa_linear_int8_grouped(count, P4(*codes), P4(*scales), None, N4(*n), x, xdt,
+                                          m, k, P4(*y), None)
+
+    assert grp(count=0) == pa.PA_ERR_INVALID_ARG
+    assert grp(count=5) == pa.PA_ERR_INVALID_ARG
+    assert grp(codes=(A, None)) == pa.PA_ERR_INVALID_ARG
+    assert grp(n=(64, 24)) == pa.PA_ERR_UNSUPPORTED      # n % 16
+    assert grp(k=96) == pa.PA_ERR_UNSUPPORTED            # k % 64
+    assert grp(codes=(A, A + 8)) == pa.PA_ERR_INVALID_ARG
+    assert grp(y=(A + 1, A)) == pa.PA_ERR_INVALID_ARG
+    assert grp(x=A + 4) == pa.PA_ERR_INVALID_ARG
+    assert grp(xdt=pa.PA_I8) == pa.PA_ERR_UNSUPPORTED
+
     q = lib.pa_linear_int8_quantize
     assert q(None, pa.PA_BF16, 16, 64, A, A, None) == pa.PA_ERR_INVALID_ARG
     assert q(A, pa.PA_I8, 16, 64, A, A, None) == pa.PA_ERR_UNSUPPORTED

@@ -147,51 +147,16 @@ def test_json_line_int8_linear(host_cuda, monkeypatch):
     monkeypatch.setattr(torch, "randint", lambda *a, device=None, **k: randint(*a, **k))
     monkeypatch.setattr(torch, "rand", lambda *a, device=None, **k: rand(*a, **k))
     monkeypatch.setattr(torch, "randn", lambda *a, device=None, **k: randn(*a, **k))
-    monkeypatch.setattr(L, "int8_linear", lambda codes, scales, x, out=None, **k: out)
-    monkeypatch.setattr(L, "int8_workspace_bytes", lambda m, n, k: 4 * m * n if n == 4096 else 0)
+    monkeypatch.setattr(L, "int8_linear_grouped", lambda mats, x, outs=None, **k: outs)
     steps = 3
     line = _run(monkeypatch, ["--workload", "int8-linear", "--layers", "1", "--num-seqs", "2",
                               "--steps", str(steps), "--warmup", "3", "--cpu-budget", "0.3"])
-    shapes = bench.LINEAR_SHAPES
+    groups = bench.LINEAR_GROUPS
     assert line["config"]["workload"] == "int8-linear" and line["config"]["tokens"] == 2
-    assert abs(line["value"] - bench.linear_bytes(2, shapes) / (STEP_MS * 1e-3) / 1e9) < 1e-9
-    # one launch per matrix plus a reduce for each split one (the 4096-channel ones)
-    assert line["gpu_launches"] == steps * (len(shapes) + 5)
+    assert abs(line["value"] - bench.linear_bytes(2, groups) / (STEP_MS * 1e-3) / 1e9) < 1e-9
+    # one grouped launch per group: the k splits are merged inside it
+    assert line["gpu_launches"] == steps * len(groups)
     assert line["roofline"]["traffic"] is None  # recorded for the four-layer, 8-token stack
-    assert line["e2e"]["h2d_bytes_per_step"] == sum(2 * 2 * k for _, k in shapes)
-    assert line["e2e"]["d2h_bytes_per_step"] == sum(2 * 2 * n for n, _ in shapes)
+    assert line["e2e"]["h2d_bytes_per_step"] == sum(2 * 2 * grp[0][1] for grp in groups)
+    assert line["e2e"]["d2h_bytes_per_step"] == sum(2 * 2 * n for grp in groups for n, _ in grp)
     assert line["cpu_baseline"]["kind"] == "oracle"
-
-
-def test_json_line_with_other_workloads(host_cuda, monkeypatch):
-    """The default run adds a "workloads" object: every other configuration's
-    value, timing, roofline, clocks and L2-flush status, timed the same way."""
-    line = _run(monkeypatch, ["--workload", "mha-7b", "--num-seqs", "2", "--steps", "4",
-                              "--warmup", "3", "--no-cpu-baseline",
-                              "--extra-workloads", "int8-kv,qwen2.5-1.5b"])
-    assert line["config"]["workload"] == "mha-7b"
-    assert set(line["workloads"]) == {"int8-kv", "qwen2.5-1.5b"}
-    for name, x in line["workloads"].items():
-        w = I.make_workload(name, seed=0, num_seqs=2)
-        assert x["config"]["workload"] == name
-        assert x["steps"] == bench.EXTRA_MIN_STEPS and x["warmup"] == 3
-        assert abs(x["ms_per_step"] - STEP_MS) < 1e-12
-        assert abs(x["value"] - w.kv_bytes() / (STEP_MS * 1e-3) / 1e9) < 1e-9
-        assert abs(x["steps_per_s"] - 1e3 / STEP_MS) < 1e-9
-        assert x["roofline"]["bound"] == "hbm" and x["roofline"]["frac"] > 0
-        assert x["l2_flushed"] == bench.needs_l2_flush(w)
-        assert set(x["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
-
-
-def test_reference_line_reports_what_it_measured(monkeypatch):
-    """--impl reference: ms_per_step is the oracle's measured time per sampled
-    step, and value is the sample's bytes over that time (no projection)."""
-    times = iter([0.0, 0.5] * 100)
-    monkeypatch.setattr(bench.time, "perf_counter", lambda: next(times))
-    line = _run(monkeypatch, ["--impl", "reference", "--workload", "tiny", "--steps", "3",
-                              "--warmup", "1", "--cpu-budget", "100"])
-    assert line["impl"] == "reference"
-    assert abs(line["ms_per_step"] - 500.0) < 1e-9   # each sampled step took 0.5 s
-    sample = line["config"]["sample_bytes_per_step"]
-    assert abs(line["value"] - sample / 0.5 / 1e9) < 1e-12
-    assert line["e2e"]["value"] == line["value"]

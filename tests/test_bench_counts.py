@@ -55,16 +55,16 @@ def test_counts_match_brute_force(name, kw):
 
 
 def test_linear_bytes_by_definition():
-    """Every code byte and fp32 scale once, the 16-bit activations in and the
-    outputs out, summed over the projections."""
+    """Every code byte and fp32 scale once, each group's 16-bit activations in
+    once (its matrices share them) and every output out."""
     m = 5
-    shapes = [(48, 64), (16, 128)]
+    groups = [[(48, 64), (32, 64)], [(16, 128)]]
     expect = 0
-    for n, k in shapes:
-        codes, scales = n * k * 1, n * 4
-        acts_in, outs = m * k * 2, m * n * 2
-        expect += codes + scales + acts_in + outs
-    assert bench.linear_bytes(m, shapes) == expect
+    for grp in groups:
+        expect += m * grp[0][1] * 2                 # the group's activations
+        for n, k in grp:
+            expect += n * k * 1 + n * 4 + m * n * 2  # codes, scales, outputs
+    assert bench.linear_bytes(m, groups) == expect
 
 
 def test_recorded_traffic_only_for_unchanged_sources(tmp_path, monkeypatch):

@@ -166,8 +166,9 @@ def test_revived_prefix_blocks_after_the_request_ended(dtype, olib):
     """"llminfer", Prefix KV cache reuse: r1 writes and publishes its prompt,
     decodes and finishes; an unrelated request then needs more blocks than are
     free, so the cache gives back r1's last prompt block (least recently used);
-    r2 with r1's prompt attaches the first five blocks from the cache and
-    appends its own tokens.  Decode of both live requests matches the oracle."""
+    r2 with r1's prompt attaches the first five blocks from the cache, the other
+    request rolls back three blocks, and r2 appends its own tokens.  Decode of
+    both live requests matches the oracle."""
     cache_dt, q_dt = (dtype.split("-") + [None])[:2]
     q_dt = q_dt or cache_dt
     src = "bf16"
@@ -198,6 +199,7 @@ def test_revived_prefix_blocks_after_the_request_ended(dtype, olib):
     add(1, 16 * (nb - 6 + 1), 20)                 # all free blocks and one cached one
     assert bm.stats()["reclaimed_blocks"] == 1
     assert bm.attach_prefix(2, keys) == 5         # the prompt's last block was reclaimed
+    bm.rollback(1, 48)                            # the other request gives back 3 blocks
     add(2, 20, 30)                                # r2 recomputes the rest of its prompt
     add(1, 1, 40)
     add(2, 1, 42)

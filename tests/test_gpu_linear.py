@@ -72,9 +72,9 @@ def test_linear_chain_shares_workspace(olib):
     dtype = "bf16"
     shapes = [(8, 4096, 4096), (8, 1024, 11008), (3, 2048, 1024), (8, 5120, 640),
               (12, 9728, 576), (8, 4096, 4096)]
+    # some of these calls split k (merged in the launch: no workspace needed)
     nbytes = max(L.int8_workspace_bytes(m, n, k) for m, n, k in shapes)
-    assert nbytes > 0                             # some of these calls split k
-    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
     mats = []
     for i, (m, n, k) in enumerate(shapes):
         w = _weights(n, k, dtype, 100 + i)
@@ -104,3 +104,36 @@ def test_linear_rejects_bad_shapes_and_alignment():
     with pytest.raises(pa.PaError) as e:          # x not 16-byte aligned
         L.int8_linear(codes, scales, xb)
     assert e.value.status == pa.PA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("m,group,k", [
+    (8, [4096, 4096, 4096], 4096),     # a 7B layer's q, k and v
+    (8, [11008, 11008], 4096),         # gate and up
+    (1, [16, 48, 1008, 336], 640),     # four ragged matrices, few channels: k split
+    (13, [4096], 11008),               # one matrix, two token groups
+    (3, [32, 16], 65536),              # very few channels over a long k: 8 splits
+])
+def test_grouped_linear_matches_oracle(dtype, m, group, k, olib):
+    """One launch for the matrices that read the same activations; every
+    output against the oracle, with a bias on every other matrix."""
+    x = I.normal_bits((m, k), dtype, 21, m + k)
+    xt = bits_to_torch(x, dtype)
+    mats, refs = [], []
+    for i, n in enumerate(group):
+        w = _weights(n, k, dtype, 50 + i + k)
+        bias = I.normal_bits((n,), dtype, 22, i) if i % 2 else None
+        codes, scales = L.int8_quantize(bits_to_torch(w, dtype))
+        mats.append((codes, scales, bits_to_torch(bias, dtype) if bias is not None else None))
+        refs.append(oracle.linear_int8(codes.cpu().numpy(), scales.cpu().numpy(), x, dtype,
+                                       bias_bits=bias, lib=olib))
+    for rep in range(2):
+        outs = L.int8_linear_grouped(mats, xt)
+        torch.cuda.synchronize()
+        for i, (y, ref) in enumerate(zip(outs, refs)):
+            assert y.shape == (m, group[i]) and y.dtype == TORCH_DT[dtype]
+            assert_close(y.double().cpu().numpy(), ref, "group %s matrix %d" % (group, i))
+        if rep == 0:
+            first = [y.clone() for y in outs]
+        else:
+            assert all(torch.equal(a, b) for a, b in zip(first, outs))  # same bits again

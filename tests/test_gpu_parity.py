@@ -120,8 +120,11 @@ DECODE_CASES = [
     ("qwen2.5-1.5b", dict(num_seqs=4, window=300), 0),
     ("mha-7b", dict(num_seqs=3, lens=("uniform", 1, 700)), 0),
     ("mha-7b", dict(num_seqs=2, lens=("uniform", 600, 1500)), 3),  # forced small partitions
+    ("mha-7b", dict(num_seqs=2, lens=("uniform", 600, 1500)), -5),  # 5-CTA clusters
+    ("qwen2.5-1.5b", dict(num_seqs=3, window=700), -16),           # 16-CTA clusters
     ("int8-kv", dict(num_seqs=5, lens=("uniform", 1, 900)), 0),
     ("int8-kv", dict(num_seqs=3, lens=("uniform", 200, 700), window=100), 2),
+    ("int8-kv", dict(num_seqs=3, lens=("uniform", 200, 700), window=100), -4),
     ("mixed", dict(num_seqs=6, num_chunks=1, chunk_len=20, lens=("uniform", 1, 2000)), 0),
 ]
 
@@ -154,29 +157,31 @@ def test_decode_shapes(D, dtype, G, olib):
     cache_o, kh, vh = oracle_cache(olib, w)
     q, ref = oracle_ref(olib, w, cache_o, [0, 1, 2], sm)
     cache, _ = device_history(w, kh, vh)
-    for pb in (0, 1, 2):
+    for pb in (0, 1, 2, -3, -16):  # workspace merges and cluster merges
         got, flags = run_decode(w, cache, q, sm, partition_blocks=pb)
         assert flags == 0
         assert_close(got, ref, "%s D=%d G=%d pb=%d" % (dtype, D, G, pb))
 
 
-def test_decode_block_relabelling_bit_identical(olib):
+@pytest.mark.parametrize("pb", [4, -6])
+def test_decode_block_relabelling_bit_identical(pb, olib):
     w = I.make_workload("int8-kv", seed=3, num_seqs=4, lens=("uniform", 50, 600))
     cache_o, kh, vh = oracle_cache(olib, w)
     q = I.query_rows(w)
     sm = 0.1
     cache, _ = device_history(w, kh, vh)
-    a, fa = run_decode(w, cache, q, sm, partition_blocks=4)
+    a, fa = run_decode(w, cache, q, sm, partition_blocks=pb)
     perm = np.random.default_rng(1).permutation(w.num_blocks).astype(np.int32)
     w2 = I.make_workload("int8-kv", seed=3, num_seqs=4, lens=("uniform", 50, 600))
     w2.block_tables = np.where(w.block_tables >= 0, perm[np.maximum(w.block_tables, 0)], -1)
     cache2, _ = device_history(w2, kh, vh)
-    b, fb = run_decode(w2, cache2, q, sm, partition_blocks=4)
+    b, fb = run_decode(w2, cache2, q, sm, partition_blocks=pb)
     assert fa == fb == 0
     assert (a == b).all()
 
 
-def test_decode_empty_and_bad_data(olib):
+@pytest.mark.parametrize("pb", [0, -3])
+def test_decode_empty_and_bad_data(pb, olib):
     """L = 0 gives zeros; a block id outside the pool drops its keys and sets
     PA_FLAG_BLOCK_ID; a context length above the table's reach is cut and sets
     PA_FLAG_CONTEXT_LEN -- both as the oracle's reading says."""
@@ -189,14 +194,14 @@ def test_decode_empty_and_bad_data(olib):
     w.block_tables = w.block_tables.copy()
     w.block_tables[3, 1] = w.num_blocks + 100
     _, ref = oracle_ref(olib, w, cache_o, [0, 1, 2, 3], 0.125)
-    got, flags = run_decode(w, cache, q, 0.125)
+    got, flags = run_decode(w, cache, q, 0.125, partition_blocks=pb)
     assert flags == pa.PA_FLAG_BLOCK_ID
     assert (got[0] == 0).all()
     assert_close(got, ref, "bad block id")
     w.block_tables[3, 1] = w.block_tables[3, 0]  # restore a valid id
     w.context_lens[2] = 10 ** 6
     _, ref = oracle_ref(olib, w, cache_o, [0, 1, 2, 3], 0.125)
-    got, flags = run_decode(w, cache, q, 0.125)
+    got, flags = run_decode(w, cache, q, 0.125, partition_blocks=pb)
     assert flags & pa.PA_FLAG_CONTEXT_LEN
     assert_close(got[[0, 1, 3]], ref[[0, 1, 3]], "clamped length")
 

@@ -23,9 +23,12 @@ from gpu_util import (ATOL, RTOL, assert_close, bits_to_torch, device_history, i
 pytestmark = pytest.mark.gpu
 
 
+# Batches with so few (sequence, kv head) units that the decode splits their
+# contexts further than a thread-block cluster can merge: the split-K partials
+# go through the scratch.
 @pytest.mark.parametrize("name,kw", [
-    ("mha-7b", dict(num_seqs=6, lens=("uniform", 1500, 4096))),
-    ("int8-kv", dict(num_seqs=5, lens=("uniform", 700, 3000))),
+    ("qwen2.5-1.5b", dict(num_seqs=2, lens=("uniform", 1500, 4096))),
+    ("int8-kv", dict(num_seqs=1, lens=("uniform", 3000, 8000))),
 ])
 def test_noalloc_matches_pa_decode_twice(name, kw, olib):
     _build.build()
@@ -64,11 +67,11 @@ def test_noalloc_rejects_batches_beyond_its_scratch():
     _build.build()
     w = I.make_workload("int8-kv", seed=1, num_seqs=2, lens=("fixed", [16, 16]))
     cache, _ = device_history(w)
-    B = 4096  # partials of 4096 seqs x 32 heads x 16 partitions exceed the scratch
-    assert pa.pa_decode_workspace_bytes(B, 32, 8, 128, 512, 0) > pa.PA_NOALLOC_SCRATCH_BYTES
-    q = torch.zeros((B, 32, 128), dtype=torch.bfloat16, device="cuda")
+    B, MB = 1, 65536  # one sequence of up to 1M tokens: 1024 partitions of 64 blocks
+    assert pa.pa_decode_workspace_bytes(B, 64, 8, 128, MB, 0) > pa.PA_NOALLOC_SCRATCH_BYTES
+    q = torch.zeros((B, 64, 128), dtype=torch.bfloat16, device="cuda")
     out = torch.empty_like(q)
-    tables = torch.zeros((B, 512), dtype=torch.int32, device="cuda")
+    tables = torch.zeros((B, MB), dtype=torch.int32, device="cuda")
     lens = torch.ones(B, dtype=torch.int32, device="cuda")
     with pytest.raises(pa.PaError) as e:
         pa.pa_decode_noalloc(cache, out, q, tables, lens, 0.1, 0, new_err())

@@ -54,22 +54,22 @@ def test_full_size_step_sampled(name, olib):
 
 
 def test_full_size_int8_linear(olib):
-    """The int8-linear workload's first layer exactly as the benchmark draws it
-    (q, k, v, o 4096x4096; gate, up 11008x4096; down 4096x11008; 8 tokens), run
-    back to back through one shared workspace as the benchmark runs them; every
-    output element against the oracle."""
+    """The int8-linear workload's first layer exactly as the benchmark draws and
+    runs it: grouped launches (q, k, v 4096x4096; o; gate, up 11008x4096; down
+    4096x11008), 8 tokens; every output element against the oracle."""
     from gpu_util import assert_close
     from paged_kv_cache_240_gb300 import _build
     from paged_kv_cache_240_gb300 import linear as L
     _build.build()
     m = 8
-    mats = bench.linear_layers(torch, bench.LINEAR_SHAPES, m, SEED)
-    nbytes = max(L.int8_workspace_bytes(m, n, k) for n, k in bench.LINEAR_SHAPES)
-    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
-    for codes, scales, x, y in mats:
-        L.int8_linear(codes, scales, x, out=y, workspace=ws)
+    layer = bench.linear_layers(torch, bench.LINEAR_GROUPS, m, SEED)
+    for x, mats in layer:
+        L.int8_linear_grouped([(c, s, None) for c, s, _ in mats], x, outs=[y for _, _, y in mats])
     torch.cuda.synchronize()
-    for (codes, scales, x, y), (n, k) in zip(mats, bench.LINEAR_SHAPES):
-        ref = oracle.linear_int8(codes.cpu().numpy(), scales.cpu().numpy(), bits(x), "bf16",
-                                 lib=olib)
-        assert_close(y.double().cpu().numpy(), ref, "int8 linear %d tokens, n=%d k=%d" % (m, n, k))
+    for x, mats in layer:
+        for codes, scales, y in mats:
+            n, k = codes.shape
+            ref = oracle.linear_int8(codes.cpu().numpy(), scales.cpu().numpy(), bits(x), "bf16",
+                                     lib=olib)
+            assert_close(y.double().cpu().numpy(), ref,
+                         "int8 linear %d tokens, n=%d k=%d" % (m, n, k))
