@@ -93,7 +93,7 @@ __device__ __forceinline__ int load_qt(uint32_t (&qb)[D / 16][2], const QT* row,
 // Output column d of O^T tile mt, C-fragment row r (0: g, 1: g+8) of thread g.
 template <int MODE, int D>
 __device__ __forceinline__ int ot_col(int mt, int g, int r) {
-  if constexpr (MODE == kI8) return (D / 8) * g + 2 * mt + r;
+  if constexpr (MODE == kI8) return 16 * mt + 2 * g + r;
   else return 16 * mt + 8 * r + g;
 }
 
@@ -263,37 +263,25 @@ __device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2]
       mma16816<BF>(o[mt], a, pb0, pb1);
     }
   } else {
-    // Thread (g, t) reads bytes [W*4*g, W*4*g + W*4) of V rows 2t, 2t+1, 2t+8,
-    // 2t+9; tile mt's rows g and g+8 are columns (D/8)*g + 2mt and +1.
-    constexpr int W = D / 32;
-    const uint8_t* vt = stage + T::kTileBytes;
-    uint32_t R[4][W];
-    const int toks[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+    // ldmatrix.trans on 16-bit pairs of codes: matrix (tokens 8j..8j+7, bytes
+    // 16mt..16mt+15) gives thread (g, t) tokens 8j+2t, 8j+2t+1 at d = 16mt+2g and
+    // +1; one byte permute per f16 pair (code + 1152) makes the A fragment of
+    // tile mt, whose rows g and g+8 are d = 16mt+2g and 16mt+2g+1
+    const int vrow = 8 * (mi & 1) + mr;
 #pragma unroll
-    for (int j = 0; j < 4; j++) {
-      if constexpr (W == 4) {
-        const uint4 v4 = *reinterpret_cast<const uint4*>(vt + T::off(toks[j], 16 * g));
-        R[j][0] = v4.x ^ 0x80808080u;
-        R[j][1] = v4.y ^ 0x80808080u;
-        R[j][2] = v4.z ^ 0x80808080u;
-        R[j][3] = v4.w ^ 0x80808080u;
-      } else {
-        const uint2 v2 = *reinterpret_cast<const uint2*>(vt + T::off(toks[j], 8 * g));
-        R[j][0] = v2.x ^ 0x80808080u;
-        R[j][1] = v2.y ^ 0x80808080u;
-      }
-    }
+    for (int mp = 0; mp < D / 32; mp++) {
+      uint32_t r[4];
+      ldsm_x4_t(r, vbase + T::off(vrow, 32 * mp + 16 * (mi >> 1)));
 #pragma unroll
-    for (int mt = 0; mt < D / 16; mt++) {
-      uint32_t a[4];
-      if (mt & 1) {
-        biased_i8_pairs_plus1152<2>(R[0][mt >> 1], R[1][mt >> 1], a[0], a[1]);
-        biased_i8_pairs_plus1152<2>(R[2][mt >> 1], R[3][mt >> 1], a[2], a[3]);
-      } else {
-        biased_i8_pairs_plus1152<0>(R[0][mt >> 1], R[1][mt >> 1], a[0], a[1]);
-        biased_i8_pairs_plus1152<0>(R[2][mt >> 1], R[3][mt >> 1], a[2], a[3]);
+      for (int h = 0; h < 2; h++) {
+        const uint32_t x0 = r[2 * h] ^ 0x80808080u, x1 = r[2 * h + 1] ^ 0x80808080u;
+        uint32_t a[4];
+        a[0] = __byte_perm(x0, 0x64646464u, 0x4240);  // row g:   tokens 2t, 2t+1
+        a[1] = __byte_perm(x0, 0x64646464u, 0x4341);  // row g+8: tokens 2t, 2t+1
+        a[2] = __byte_perm(x1, 0x64646464u, 0x4240);  // row g:   tokens 2t+8, 2t+9
+        a[3] = __byte_perm(x1, 0x64646464u, 0x4341);  // row g+8: tokens 2t+8, 2t+9
+        mma16816<false>(o[2 * mp + h], a, pb0, pb1);
       }
-      mma16816<false>(o[mt], a, pb0, pb1);
     }
   }
 }
