@@ -9,6 +9,8 @@
 // elements.  Bit-exactness with the CPU oracle rests on three facts: 16-bit ->
 // fp32 conversion is exact, fmaxf/fabsf are exact, and __fdiv_rn and
 // __float2int_rn are the IEEE round-to-nearest(-even) operations the oracle uses.
+#include <type_traits>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -47,6 +49,11 @@ __global__ void __launch_bounds__(kWriteWarps * 32) write_copy_kernel(WriteParam
   const long long row = (long long)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
   if (row >= (long long)p.num_tokens * p.num_kv_heads) return;
   const int t = (int)(row / p.num_kv_heads), h = (int)(row % p.num_kv_heads);
+  // the row's bits are read together with its slot (neither waits for the other)
+  constexpr int kBytes = D * 2;
+  using V = typename std::conditional<kBytes / 32 == 8, uint2, uint32_t>::type;  // 8 or 4 B a lane
+  const V kv = reinterpret_cast<const V*>(p.k + row * kBytes)[lane];
+  const V vv = reinterpret_cast<const V*>(p.v + row * kBytes)[lane];
   const int32_t slot = p.slot_mapping[t];
   if (slot < 0) return;
   if ((long long)slot >= (long long)p.num_blocks * kBlock) {
@@ -54,20 +61,8 @@ __global__ void __launch_bounds__(kWriteWarps * 32) write_copy_kernel(WriteParam
     return;
   }
   const long long dst_row = ((long long)(slot / kBlock) * p.num_kv_heads + h) * kBlock + slot % kBlock;
-  constexpr int kBytes = D * 2;
-  if constexpr (kBytes / 32 == 8) {  // D = 128: 8 bytes per lane
-    const uint2* ks = reinterpret_cast<const uint2*>(p.k + row * kBytes);
-    const uint2* vs = reinterpret_cast<const uint2*>(p.v + row * kBytes);
-    uint2 kv = ks[lane], vv = vs[lane];
-    reinterpret_cast<uint2*>(p.k_cache + dst_row * kBytes)[lane] = kv;
-    reinterpret_cast<uint2*>(p.v_cache + dst_row * kBytes)[lane] = vv;
-  } else {  // D = 64: 4 bytes per lane
-    const uint32_t* ks = reinterpret_cast<const uint32_t*>(p.k + row * kBytes);
-    const uint32_t* vs = reinterpret_cast<const uint32_t*>(p.v + row * kBytes);
-    uint32_t kv = ks[lane], vv = vs[lane];
-    reinterpret_cast<uint32_t*>(p.k_cache + dst_row * kBytes)[lane] = kv;
-    reinterpret_cast<uint32_t*>(p.v_cache + dst_row * kBytes)[lane] = vv;
-  }
+  reinterpret_cast<V*>(p.k_cache + dst_row * kBytes)[lane] = kv;
+  reinterpret_cast<V*>(p.v_cache + dst_row * kBytes)[lane] = vv;
 }
 
 // Quantise one row held as E = D/32 consecutive elements per lane.
@@ -98,6 +93,13 @@ __global__ void __launch_bounds__(kWriteWarps * 32) write_quant_kernel(WritePara
   const long long row = (long long)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
   if (row >= (long long)p.num_tokens * p.num_kv_heads) return;
   const int t = (int)(row / p.num_kv_heads), h = (int)(row % p.num_kv_heads);
+  // the K and V rows are read together with the slot (neither waits for the other)
+  using R = typename std::conditional<E == 4, uint2, uint32_t>::type;
+  R raw[2];
+#pragma unroll
+  for (int which = 0; which < 2; which++)
+    raw[which] =
+        *reinterpret_cast<const R*>(reinterpret_cast<const IT*>(which ? p.v : p.k) + row * D + lane * E);
   const int32_t slot = p.slot_mapping[t];
   if (slot < 0) return;
   if ((long long)slot >= (long long)p.num_blocks * kBlock) {
@@ -107,19 +109,10 @@ __global__ void __launch_bounds__(kWriteWarps * 32) write_quant_kernel(WritePara
   const long long dst_row = ((long long)(slot / kBlock) * p.num_kv_heads + h) * kBlock + slot % kBlock;
 #pragma unroll
   for (int which = 0; which < 2; which++) {
-    const IT* src = reinterpret_cast<const IT*>(which ? p.v : p.k) + row * D + lane * E;
     float x[E];
-    if constexpr (E == 4) {
-      uint2 raw = *reinterpret_cast<const uint2*>(src);
-      const IT* e = reinterpret_cast<const IT*>(&raw);
+    const IT* e = reinterpret_cast<const IT*>(&raw[which]);
 #pragma unroll
-      for (int i = 0; i < 4; i++) x[i] = in_to_f32<IT>(e[i]);
-    } else {
-      uint32_t raw = *reinterpret_cast<const uint32_t*>(src);
-      const IT* e = reinterpret_cast<const IT*>(&raw);
-#pragma unroll
-      for (int i = 0; i < E; i++) x[i] = in_to_f32<IT>(e[i]);
-    }
+    for (int i = 0; i < E; i++) x[i] = in_to_f32<IT>(e[i]);
     int8_t q[E];
     float scale;
     quantize_row<E>(x, q, scale);
