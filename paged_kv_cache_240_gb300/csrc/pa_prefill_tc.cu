@@ -321,15 +321,16 @@ struct Item {
   int n, kvh, q0, C, L, R0, nrows, lo_u, hi_u, first, ntiles;
 };
 
-__device__ __forceinline__ Item item_info(const AttnParams& p, int n, int kvh, int tile,
-                                          bool report) {
+// The item from its sequence's raw lengths (q0, q1 = cu_q_lens[n], cu_q_lens[n+1],
+// Lraw = context_lens[n]), with the checks of clamp_context.
+__device__ __forceinline__ Item item_make(const AttnParams& p, int n, int kvh, int tile, int q0,
+                                          int q1, int Lraw, bool report) {
   Item it;
   it.valid = false;
   it.ntiles = 0;
   it.n = n;
   it.kvh = kvh;
   report = report && kvh == 0 && tile == 0;  // one report per sequence
-  const int q0 = p.cu_q_lens[it.n], q1 = p.cu_q_lens[it.n + 1];
   if (q0 < 0 || q1 < q0 || q1 > p.num_q_tokens) {
     if (report) set_flag(p.err, PA_FLAG_Q_LEN);
     return it;
@@ -339,7 +340,12 @@ __device__ __forceinline__ Item item_info(const AttnParams& p, int n, int kvh, i
     if (report) set_flag(p.err, PA_FLAG_Q_LEN);
     C = p.max_q_len;
   }
-  const int L = clamp_context(p, it.n, report);
+  const int cap = p.max_blocks_per_seq * kBlock;
+  int L = Lraw;
+  if (L < 0 || L > cap) {
+    if (report) set_flag(p.err, PA_FLAG_CONTEXT_LEN);
+    L = L < 0 ? 0 : cap;
+  }
   if (C > L && report) set_flag(p.err, PA_FLAG_Q_LEN);
   it.q0 = q0;
   it.C = C;
@@ -358,6 +364,12 @@ __device__ __forceinline__ Item item_info(const AttnParams& p, int n, int kvh, i
   return it;
 }
 
+__device__ __forceinline__ Item item_info(const AttnParams& p, int n, int kvh, int tile,
+                                          bool report) {
+  return item_make(p, n, kvh, tile, p.cu_q_lens[n], p.cu_q_lens[n + 1], p.context_lens[n],
+                   report);
+}
+
 // The work list: items ordered by cost (key tiles + a fixed overhead), longest
 // first, when the CTA could rank the (sequence, tile) pairs (every kv head of a
 // pair costs the same); in (sequence, kv head, tile) order otherwise.  With the
@@ -371,39 +383,43 @@ __device__ __forceinline__ Item item_info(const AttnParams& p, int n, int kvh, i
 // way CTA b's first item is position b.  Returns false past the end (or when a
 // bounded wait for the assignment ran out).
 struct WorkList {
-  const uint16_t* order;  // rank -> pair index (low 9 bits) and cost (high 7), or nullptr
-  int num_pairs, kv_heads, q_tiles;
-  bool greedy;
-  int first_items;                 // positions of cost > 0 (ranked list)
-  const volatile uint16_t* items;  // greedy: this CTA's positions
-  const volatile int* count;       // greedy: how many are published
-  const volatile int* done;        // greedy: all are published
+  // Only the CTA-wide decisions are held (in registers of every role); the
+  // ranked order [num_pairs] and the greedy positions live in shared memory at
+  // the layout's offsets, and the sizes come from the parameters.
+  bool ranked;      // the order of the pairs by cost exists
+  bool greedy;      // greedy assignment (ranked list of a key-split launch)
+  int first_items;  // positions of cost > 0 (ranked list)
 
-  __device__ __forceinline__ bool at(int j, int& n, int& kvh, int& tile) const {
+  template <class LY>
+  __device__ __forceinline__ bool at(const AttnParams& p, int num_pairs, const uint8_t* smem,
+                                     int j, int& n, int& kvh, int& tile) const {
     const int grid = gridDim.x, b = blockIdx.x;
+    const int kv_heads = p.num_kv_heads, q_tiles = p.q_tiles;
     long long s;
     if (greedy) {
+      const volatile int* count = reinterpret_cast<const volatile int*>(
+          smem + LY::kSchedOff + LY::kSchedItems * 2);
       if (j == 0) {
         if (b >= first_items) return false;
         s = b;
       } else {
         const long long t0 = clock64();
-        while (*count <= j) {
-          if (*done) {
-            if (*count <= j) return false;
+        while (count[0] <= j) {
+          if (count[1]) {  // all are published
+            if (count[0] <= j) return false;
             break;
           }
           if (clock64() - t0 > kWaitLimitCycles) return false;
         }
         __threadfence_block();
-        s = items[j];
+        s = reinterpret_cast<const volatile uint16_t*>(smem + LY::kSchedOff)[j];
       }
     } else {
       s = (long long)j * grid + ((j & 1) ? grid - 1 - b : b);
     }
     if (s >= (long long)num_pairs * kv_heads) return false;
-    if (order) {
-      const int pair = order[s / kv_heads] & 0x1FF;
+    if (ranked) {
+      const int pair = reinterpret_cast<const uint16_t*>(smem + LY::kOrderOff)[s / kv_heads] & 0x1FF;
       kvh = (int)(s % kv_heads);
       n = pair / q_tiles;
       tile = pair % q_tiles;
@@ -413,6 +429,52 @@ struct WorkList {
       kvh = (int)(s % per_seq) / q_tiles;
       tile = (int)(s % per_seq) % q_tiles;
     }
+    return true;
+  }
+  // whether position j is known without waiting (greedy: published, or the
+  // list is complete)
+  template <class LY>
+  __device__ __forceinline__ bool ready(const uint8_t* smem, int j) const {
+    if (!greedy || j == 0) return true;
+    const volatile int* count =
+        reinterpret_cast<const volatile int*>(smem + LY::kSchedOff + LY::kSchedItems * 2);
+    return count[0] > j || count[1] != 0;
+  }
+};
+
+// A role's walk over its CTA's items.  fetch() looks up the next item and
+// starts the loads of its sequence's lengths; take() hands it out (fetching
+// first if that has not happened).  Calling fetch() early -- at an item's start,
+// or after its last tile -- lets the global-memory latency pass while the
+// current item's work runs instead of at the next item's start.  A greedy
+// list publishes its positions as the scheduler warp assigns them: an early
+// fetch does not wait for one (take() will).
+template <class LY>
+struct ItemStream {
+  WorkList wl;
+  int j, n, kvh, tile, q0, q1, L;
+  bool have, fetched;
+
+  __device__ __forceinline__ explicit ItemStream(const WorkList& w) : wl(w), j(0), fetched(false) {}
+  __device__ __forceinline__ void load(const AttnParams& p, int num_pairs, const uint8_t* smem) {
+    fetched = true;
+    have = wl.template at<LY>(p, num_pairs, smem, j, n, kvh, tile);
+    if (have) {
+      q0 = p.cu_q_lens[n];
+      q1 = p.cu_q_lens[n + 1];
+      L = p.context_lens[n];
+    }
+  }
+  __device__ __forceinline__ void fetch(const AttnParams& p, int num_pairs, const uint8_t* smem) {
+    if (!fetched && wl.template ready<LY>(smem, j)) load(p, num_pairs, smem);
+  }
+  __device__ __forceinline__ bool take(const AttnParams& p, int num_pairs, const uint8_t* smem,
+                                       Item& it, bool report) {
+    if (!fetched) load(p, num_pairs, smem);
+    if (!have) return false;
+    it = item_make(p, n, kvh, tile, q0, q1, L, report);
+    j++;
+    fetched = false;
     return true;
   }
 };
@@ -497,21 +559,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   // the work order (the V stages serve as scratch: nothing has been loaded yet)
+  const int num_pairs = num_seqs * p.q_tiles;
   WorkList wl;
-  wl.num_pairs = num_seqs * p.q_tiles;
-  wl.kv_heads = p.num_kv_heads;
-  wl.q_tiles = p.q_tiles;
-  wl.order = nullptr;
+  wl.ranked = false;
   wl.greedy = false;
   wl.first_items = 0;
-  wl.items = sched_items;
-  wl.count = sched;
-  wl.done = sched + 1;
   __syncthreads();  // the scheduler's counters are set
-  if (wl.num_pairs <= kMaxPlan) {
+  if (num_pairs <= kMaxPlan) {
     int* cost = reinterpret_cast<int*>(smem + LY::kVOff);
     uint16_t* order = reinterpret_cast<uint16_t*>(smem + LY::kOrderOff);
-    for (int j = threadIdx.x; j < wl.num_pairs; j += kThreads) {
+    for (int j = threadIdx.x; j < num_pairs; j += kThreads) {
       const Item it = item_info(p, j / p.q_tiles, 0, j % p.q_tiles, false);
       const int c = it.valid ? min(it.ntiles + kItemCost, 127) : 0;
       cost[j] = c;
@@ -523,21 +580,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncthreads();
-    for (int j = threadIdx.x; j < wl.num_pairs; j += kThreads) {
+    for (int j = threadIdx.x; j < num_pairs; j += kThreads) {
       const int cj = cost[j];
       int rank = 0;
-      for (int i2 = 0; i2 < wl.num_pairs; i2++) {
+      for (int i2 = 0; i2 < num_pairs; i2++) {
         const int ci = cost[i2];
         rank += (ci > cj || (ci == cj && i2 < j)) ? 1 : 0;
       }
       order[rank] = (uint16_t)(j | (cj << 9));
     }
-    wl.order = order;
+    wl.ranked = true;
   }
   fence_before();
   __syncthreads();
   fence_after();
-  if (KS && wl.order && sched[5] > 0 && gridDim.x <= 160) {
+  if (KS && wl.ranked && sched[5] > 0 && gridDim.x <= 160) {
     // greedy (short chunks: many items of very different lengths; the long
     // chunks' few large items keep the alternating order, which measured
     // better there) when it provably fits: a CTA's work stays below
@@ -553,21 +610,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     setmaxnreg_dec<kCtlRegs>();
-    if (warp == 0) {
-      // ---------------- producer: each item's Q, then its K and V tiles
+    if (warp == 0 || warp == 3) {
+      // ---------------- producers: warp 0 loads each item's Q and its K tiles,
+      // warp 3 its V tiles, so that neither ring waits for the other's stages
+      // (a V stage frees a tile later than a K stage does)
+      const bool kprod = warp == 0;
       int gk = 0, gv = 0, k = 0;  // K tiles, V tiles and items with tiles so far
-      int n, kvh, tile;
-      for (int j = 0; !timed_out && wl.at(j, n, kvh, tile); j++) {
-        const Item it = item_info(p, n, kvh, tile, threadIdx.x == 0);
+      ItemStream<LY> items(wl);
+      Item it;
+      while (!timed_out && items.take(p, num_pairs, smem, it, threadIdx.x == 0)) {
+        items.fetch(p, num_pairs, smem);
         if (!it.valid || it.ntiles == 0) continue;
         // Q of this item, once the previous item's S MMAs have finished with it
-        if (k > 0 && !warp_wait(q_free, (k - 1) & 1)) {
+        if (kprod && k > 0 && !warp_wait(q_free, (k - 1) & 1)) {
           timed_out = true;
           break;
         }
         uint8_t* qs = smem + LY::kQOff;
         constexpr int kQLoad = KS ? 1 : kQTiles;  // key split: tile 0 only
-        if (q_tma) {
+        if (!kprod) {
+          // V producer: no Q
+        } else if (q_tma) {
           // box [128/G tokens][G heads][64 columns] = 128 rows of the tile
           if (lane == 0) mbar_arrive_expect_tx(q_full, kQLoad * LY::kQBytes);
           __syncwarp();
@@ -613,45 +676,48 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool inside = lane < kTileBlocks && kTileBlocks * t + lane < nblk;
           const int mine = inside ? from : -1;
           const bool ok = inside && mine >= 0 && mine < p.num_blocks;
-          if (inside && !ok) set_flag(p.err, PA_FLAG_BLOCK_ID);
+          if (kprod && inside && !ok) set_flag(p.err, PA_FLAG_BLOCK_ID);
           const unsigned okmask = __ballot_sync(0xffffffffu, ok);
           const uint32_t tile_bytes = __popc(okmask) * LY::kChunks * kBlock * 128;
           const int row0 = (mine * p.num_kv_heads + it.kvh) * kBlock;
-          // K of tile gk
-          const int ks = gk % kKS;
-          if (gk >= kKS && !warp_wait(&k_free[ks], ((gk / kKS) - 1) & 1)) {
-            timed_out = true;
-            break;
-          }
-          if (lane == 0) {
-            bmask[gk % kFlagRing] = okmask;
-            mbar_arrive_expect_tx(&k_full[ks], tile_bytes);
-          }
-          __syncwarp();
-          if (ok) {
-            uint8_t* kbase = smem + LY::kKOff + ks * LY::kKVBytes;
+          if (kprod) {
+            // K of tile gk
+            const int ks = gk % kKS;
+            if (gk >= kKS && !warp_wait(&k_free[ks], ((gk / kKS) - 1) & 1)) {
+              timed_out = true;
+              break;
+            }
+            if (lane == 0) {
+              bmask[gk % kFlagRing] = okmask;
+              mbar_arrive_expect_tx(&k_full[ks], tile_bytes);
+            }
+            __syncwarp();
+            if (ok) {
+              uint8_t* kbase = smem + LY::kKOff + ks * LY::kKVBytes;
 #pragma unroll
-            for (int h = 0; h < LY::kChunks; h++)
-              tma_load_2d(kbase + h * LY::kKVChunk + lane * kBlock * 128, &tmk, 64 * h, row0,
-                          &k_full[ks]);
-          }
-          gk++;
-          // V of tile gv (= gk - 1)
-          const int vs = gv % VS;
-          if (gv >= VS && !warp_wait(&v_free[vs], ((gv / VS) - 1) & 1)) {
-            timed_out = true;
-            break;
-          }
-          if (lane == 0) mbar_arrive_expect_tx(&v_full[vs], tile_bytes);
-          __syncwarp();
-          if (ok) {
-            uint8_t* vbase = smem + LY::v_off(vs);
+              for (int h = 0; h < LY::kChunks; h++)
+                tma_load_2d(kbase + h * LY::kKVChunk + lane * kBlock * 128, &tmk, 64 * h, row0,
+                            &k_full[ks]);
+            }
+            gk++;
+          } else {
+            // V of tile gv
+            const int vs = gv % VS;
+            if (gv >= VS && !warp_wait(&v_free[vs], ((gv / VS) - 1) & 1)) {
+              timed_out = true;
+              break;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(&v_full[vs], tile_bytes);
+            __syncwarp();
+            if (ok) {
+              uint8_t* vbase = smem + LY::v_off(vs);
 #pragma unroll
-            for (int h = 0; h < LY::kChunks; h++)
-              tma_load_2d(vbase + h * LY::kKVChunk + lane * kBlock * 128, &tmv, 64 * h, row0,
-                          &v_full[vs]);
+              for (int h = 0; h < LY::kChunks; h++)
+                tma_load_2d(vbase + h * LY::kKVChunk + lane * kBlock * 128, &tmv, 64 * h, row0,
+                            &v_full[vs]);
+            }
+            gv++;
           }
-          gv++;
         }
       }
       // no copy may still be landing in shared memory when the CTA exits; the
@@ -661,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&k_full[t % kKS], (t / kKS) & 1)) break;
         for (int t = gv > VS ? gv - VS : 0; t < gv; t++)
           if (!mbar_wait(&v_full[t % VS], (t / VS) & 1)) break;
-        if (k > 0 && !mbar_wait(q_full, (k - 1) & 1)) timed_out = true;
+        if (kprod && k > 0 && !mbar_wait(q_full, (k - 1) & 1)) timed_out = true;
       }
       if (timed_out && lane == 0) set_flag(p.err, PA_FLAG_TIMEOUT);
     } else if (warp == 2) {
@@ -672,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int mine = 0;
         const int grid = gridDim.x;
         for (int s = 0; s < wl.first_items; s++) {
-          const uint32_t c = wl.order[s / wl.kv_heads] >> 9;
+          const uint32_t c = reinterpret_cast<const uint16_t*>(smem + LY::kOrderOff)[s / p.num_kv_heads] >> 9;
           uint32_t best = 0xffffffffu;
 #pragma unroll
           for (int q = 0; q < 5; q++)
@@ -716,7 +782,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           return true;
         }
         const uint64_t dV = dV0 + (uint64_t)(((gg % kVS) * LY::kKVBytes) >> 4);
-        const uint32_t mask = bmask[gg % kFlagRing];
+        // lane 0's copy: the compiler sees one value for the warp
+        const uint32_t mask = __shfl_sync(0xffffffffu, bmask[gg % kFlagRing], 0);
         const uint32_t dO = tmem + q * LY::kTileCols + LY::kOCol;
         const uint32_t aP = tmem + q * LY::kTileCols + LY::kSCol;
         if (mask == 0xFFu && started) {
@@ -790,9 +857,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           return true;
         };
         int g = 0, k = 0, c0 = 0, c1 = 0;  // c_q: slot q's tiles so far
-        int n, kvh, tile;
-        for (int j = 0; ok && wl.at(j, n, kvh, tile); j++) {
-          const Item it = item_info(p, n, kvh, tile, false);
+        ItemStream<LY> items(wl);
+        Item it;
+        while (ok && items.take(p, num_pairs, smem, it, false)) {
+          items.fetch(p, num_pairs, smem);
           if (!it.valid || it.ntiles == 0) continue;
           ok = warp_wait(q_full, k & 1);
           k++;
@@ -828,9 +896,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         int g = 0, k = 0;
-        int n, kvh, tile;
-        for (int j = 0; ok && wl.at(j, n, kvh, tile); j++) {
-          const Item it = item_info(p, n, kvh, tile, false);
+        ItemStream<LY> items(wl);
+        Item it;
+        while (ok && items.take(p, num_pairs, smem, it, false)) {
+          items.fetch(p, num_pairs, smem);
           if (!it.valid || it.ntiles == 0) continue;
           ok = warp_wait(q_full, k & 1);
           k++;
@@ -838,12 +907,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           live1 = it.R0 + kRows < it.nrows;
           // Per tile g: P V of tile g-1 and S of tile g for each query tile, in the
           // order P V_0, S_0, P V_1, S_1, except that P V_1 goes first when its P is
-          // already there, so the tensor pipe always has queued work while the MMA
-          // warp waits for a P V to finish before the S that overwrites its P.
+          // already there.  The issuing thread blocks while an MMA waits for the
+          // tensor pipe, so the pipe idles whenever the warp does anything else:
+          // the wait for the next tile's K (loaded well ahead) is taken while
+          // P V_1 runs, just before the wait for it to finish.
+          if (ok) ok = warp_wait(&k_full[g % kKS], (g / kKS) & 1);
           for (int t = 0; t < it.ntiles && ok; t++, g++) {
-            ok = warp_wait(&k_full[g % kKS], (g / kKS) & 1);
             const uint64_t dK = dK0 + (uint64_t)(((g % kKS) * LY::kKVBytes) >> 4);
-            if (ok && t >= 1) {
+            const bool more = t + 1 < it.ntiles;
+            if (t >= 1) {
               ok = warp_wait(&v_full[(g - 1) % kVS], ((g - 1) / kVS) & 1);
               if (ok) ok = pv(0, g - 1, started0);
               bool pv1 = false;
@@ -854,13 +926,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (ok) ok = s_mma(0, g, dK);
               if (ok && !pv1) ok = pv(1, g - 1, started1);
               if (ok) commit_elect(&v_free[(g - 1) % kVS]);
-              if (ok) ok = s_mma(1, g, dK);
-            } else if (ok) {
+            } else {
               ok = s_mma(0, g, dK);
-              if (ok) ok = s_mma(1, g, dK);
             }
+            // the next tile's K
+            if (ok && more) ok = warp_wait(&k_full[(g + 1) % kKS], ((g + 1) / kKS) & 1);
+            if (ok) ok = s_mma(1, g, dK);
             if (ok) commit_elect(&k_free[g % kKS]);
-            if (ok && t == it.ntiles - 1) commit_elect(q_free);  // Q is no longer read
+            if (ok && !more) commit_elect(q_free);  // Q is no longer read
           }
           if (ok) {  // the item's last tile
             ok = warp_wait(&v_full[(g - 1) % kVS], ((g - 1) / kVS) & 1);
@@ -886,9 +959,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // KS: this slot's tiles so far (its barriers' phases), slot 1's tiles so far
     // (slot 0 waits on its P V), and items merged so far
     int cq = 0, c1 = 0, kk = 0;
-    int n, kvh, tile;
-    for (int j = 0; !timed_out && wl.at(j, n, kvh, tile); j++) {
-      const Item it = item_info(p, n, kvh, tile, false);
+    ItemStream<LY> items(wl);
+    Item it;
+    while (!timed_out && items.take(p, num_pairs, smem, it, false)) {
       if (!it.valid) continue;
       const int R = it.R0 + (KS ? 0 : q * kRows) + row;
       const bool rvalid = R < it.nrows;
@@ -965,21 +1038,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t mask = bmask[g % kFlagRing];
         float x[kKeys];
         tmem_ld128(lane_base + LY::kSCol, x);
-        // maximum of the scaled scores this row can see; an inner tile (every key
-        // visible to every row of the warp) skips the masks.  Eight partial maxima
-        // (three-input max) keep the dependency chains short.
-        // (rows past the chunk do not hold it back: their outputs are not stored,
-        // and each row of O depends on its own row of P only)
-        const bool inner = __all_sync(0xffffffffu, !rvalid || ((mask & 0xFFu) == 0xFFu &&
-                                                               pos0 >= row_lo &&
-                                                               pos0 + kKeys - 1 <= row_hi)) &&
-                           sc > 0.0f;
+        // maximum of the scaled scores this row can see.  With sm_scale > 0 the
+        // scores stay raw (the scale is folded into the exponent's FFMA and applied
+        // to the maximum); an inner tile (every key visible to every row of the
+        // warp) needs no mask, an edge tile masks the keys outside the row's range
+        // [a, b] and the blocks that were not loaded (the same for every row: a
+        // uniform branch per block).  Eight partial maxima (three-input max) keep
+        // the dependency chains short.  (Rows past the chunk do not hold it back:
+        // their outputs are not stored, and each row of O depends on its own row
+        // of P only.)
+        const bool raw = sc > 0.0f;
+        const bool inner = raw && (mask & 0xFFu) == 0xFFu &&
+                           __all_sync(0xffffffffu, !rvalid || (pos0 >= row_lo &&
+                                                               pos0 + kKeys - 1 <= row_hi));
         if (!inner) {
+          // keys this row sees: [a, b] of the tile (rows past the chunk: all)
+          const int a = rvalid ? row_lo - pos0 : 0, b = rvalid ? row_hi - pos0 : kKeys - 1;
+          if (raw) {
+            // 16-key blocks are classed for the whole warp (its rows' bounds differ
+            // by a few keys): masked for every row (or not loaded), visible to
+            // every row, or mixed -- only mixed blocks are masked key by key
+            uint32_t dead, mixed;  // per block: masked for every row / for some rows
+            {
+              const int amin = __reduce_min_sync(0xffffffffu, rvalid ? a : 0x7fffffff);
+              const int amax = __reduce_max_sync(0xffffffffu, rvalid ? a : (int)0x80000000);
+              const int bmin = __reduce_min_sync(0xffffffffu, rvalid ? b : 0x7fffffff);
+              const int bmax = __reduce_max_sync(0xffffffffu, rvalid ? b : (int)0x80000000);
+              dead = ~mask & 0xFFu;
+              mixed = 0u;
 #pragma unroll
-          for (int i = 0; i < kKeys; i++) {
-            const int kp = pos0 + i;
-            const bool vis = kp >= row_lo && kp <= row_hi && ((mask >> (i / kBlock)) & 1u);
-            x[i] = vis ? x[i] * sc : -INFINITY;
+              for (int s = 0; s < kTileBlocks; s++) {
+                const int i0 = kBlock * s, i1 = i0 + kBlock - 1;
+                if (i1 < amin || i0 > bmax) dead |= 1u << s;
+                if (i0 < amax || i1 > bmin) mixed |= 1u << s;
+              }
+              mixed &= ~dead;
+            }
+#pragma unroll
+            for (int s = 0; s < kTileBlocks; s++) {
+              if (((dead | mixed) >> s) & 1u) {
+                const bool d = (dead >> s) & 1u;
+                const int ea = d ? kKeys : a, eb = d ? -1 : b;
+#pragma unroll
+                for (int j = 0; j < kBlock; j++) {
+                  const int i = kBlock * s + j;
+                  x[i] = (i >= ea && i <= eb) ? x[i] : -INFINITY;
+                }
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < kKeys; i++)
+              x[i] = (i >= a && i <= b && ((mask >> (i / kBlock)) & 1u)) ? x[i] * sc : -INFINITY;
           }
         }
         float pm[8];
@@ -990,7 +1100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 8; j++) pm[j] = fmax3(pm[j], x[16 * k16 + j], x[16 * k16 + 8 + j]);
         float mt = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
-        if (inner) mt *= sc;
+        if (raw) mt *= sc;
         // lazy rescale: only when this row's maximum grew by more than 2^8 (O is
         // scaled below, once the scores are no longer held in registers)
         const bool need = mt > m_used + kLazyRescale;
@@ -1002,10 +1112,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= factor;
           m_used = m_new;
         }
-        // inner tiles hold raw scores (the scale is folded into one FFMA), edge
-        // tiles already-scaled ones (-inf where masked); pairs of keys share one
-        // packed FMA and one packed add into four pairs of partial sums
-        const unsigned long long mul2 = f2pack(inner ? sc : 1.0f, inner ? sc : 1.0f);
+        // raw scores (-inf where masked) take the scale in one FFMA, prescaled
+        // ones (sm_scale <= 0) do not; pairs of keys share one packed FMA and one
+        // packed add into four pairs of partial sums
+        const unsigned long long mul2 = f2pack(raw ? sc : 1.0f, raw ? sc : 1.0f);
         const unsigned long long sub2 = f2pack(-m_used, -m_used);
         unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[kKeys / 2];
@@ -1051,6 +1161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&p_full[q]);
       }
       if (timed_out) break;
+      items.fetch(p, num_pairs, smem);  // the next item's lengths load during the epilogue
       if constexpr (KS) {
         if (q == 1) {
           // slot 1, if it had tiles: hand (m, l) to slot 0, which reads O_1; the
