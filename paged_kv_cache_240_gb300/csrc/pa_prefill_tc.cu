@@ -16,11 +16,12 @@
 // per key of a 64-key tile with P in shared memory; shared-memory bandwidth, not
 // the tensor core, bounded that design.
 //
-// Warps: warpgroup 0 = warp 0 the TMA producer (Q, and K and V tiles into separate
-// rings), warp 1 the MMA warp (it runs the schedule, one elected lane issues) and
-// tensor-memory owner, warps 2-3 idle; warpgroups 1 and 2 = softmax of query tiles
-// 0 and 1, one TMEM lane (row) per thread.  Registers move from warpgroup 0 to
-// the softmax warpgroups (setmaxnreg), which hold a row's 128 scores.
+// Warps: warpgroup 0 = warp 0 the Q and K producer, warp 3 the V producer (TMA
+// into separate rings, each paced only by its own ring), warp 1 the MMA warp (it
+// runs the schedule, one elected lane issues) and tensor-memory owner, warp 2 the
+// scheduler of the key-split instance; warpgroups 1 and 2 = softmax of query
+// tiles 0 and 1, one TMEM lane (row) per thread.  Registers move from warpgroup 0
+// to the softmax warpgroups (setmaxnreg), which hold a row's 128 scores.
 //
 // MMA order per key tile t:  P V_0 of tile t-1, S_0 of t, P V_1 of t-1, S_1 of t
 // (P V_1 moves ahead of S_0 when its P is ready).  S_q of tile t overwrites the
@@ -171,6 +172,7 @@ __device__ __forceinline__ bool warp_test(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
+
 
 __device__ __forceinline__ void fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
