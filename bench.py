@@ -345,9 +345,11 @@ def time_ours(args, w, torch, pa, I, rank, world, steps=None, warmup=None):
         run_step, run_dec, run_pre = step, st.decode, st.prefill
     else:
         g_step = capture(torch, step, stream)
-        g_dec = capture(torch, st.decode, stream)
+        # a call with nothing to do (no decoding sequence, or no chunk) is not captured
+        g_dec = capture(torch, st.decode, stream) if st.nd else None
         g_pre = capture(torch, st.prefill, stream) if st.max_q else None
-        run_step, run_dec = g_step.replay, g_dec.replay
+        run_step = g_step.replay
+        run_dec = g_dec.replay if g_dec else (lambda: None)
         run_pre = g_pre.replay if g_pre else (lambda: None)
     try:
         uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
@@ -375,7 +377,7 @@ def time_ours(args, w, torch, pa, I, rank, world, steps=None, warmup=None):
         clk = clocks.stop()
         # the two attention calls on their own, for the per-kernel roofline
         nk = max(3, min(steps, 500))
-        dec_ms = time_replays(torch, stream, run_dec, nk, flush)
+        dec_ms = time_replays(torch, stream, run_dec, nk, flush) if st.nd else [0.0]
         pre_ms = time_replays(torch, stream, run_pre, nk, flush) if st.max_q else [0.0]
         # the same step launched call by call from Python, for comparison with the
         # graph replays above
