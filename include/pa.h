@@ -37,6 +37,9 @@
  *     scale = amax / 127 (fp32 IEEE division) and code = x / scale (fp32 IEEE
  *     division) rounded half to even and clamped to [-127, 127]; amax = 0 gives
  *     scale 0 and zero codes.  K and V have separate scales per (token, kv head).
+ *     Each code is stored as one offset-binary byte, code + 128 (the code's
+ *     two's-complement byte with its top bit flipped): the readers turn bytes
+ *     into exact f16 operands (1024 + byte) without a sign fix-up.
  *   - Supported: block_size 16, head_dim 64 or 128, 16-bit caches (fp16, bf16)
  *     with q of the same type, int8 caches with fp16 or bf16 q.  `out` has q's
  *     type.  Every device pointer must be 16-byte aligned.

@@ -297,13 +297,13 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
     for (int c = 0; c < D / 16; c += 2) {
       uint32_t r[4], lo, hi;
       ldsm_x4(r, kbase + T::off(krow, 16 * (c + (mi & 1))));
-      biased_i8x4_to_f16(r[0] ^ 0x80808080u, lo, hi);
+      biased_i8x4_to_f16(r[0], lo, hi);
       mma16816<false>(s[0], qa[c], lo, hi);
-      biased_i8x4_to_f16(r[1] ^ 0x80808080u, lo, hi);
+      biased_i8x4_to_f16(r[1], lo, hi);
       mma16816<false>(s[0], qa[c + 1], lo, hi);
-      biased_i8x4_to_f16(r[2] ^ 0x80808080u, lo, hi);
+      biased_i8x4_to_f16(r[2], lo, hi);
       mma16816<false>(s[1], qa[c], lo, hi);
-      biased_i8x4_to_f16(r[3] ^ 0x80808080u, lo, hi);
+      biased_i8x4_to_f16(r[3], lo, hi);
       mma16816<false>(s[1], qa[c + 1], lo, hi);
     }
   }
@@ -449,14 +449,14 @@ __device__ __forceinline__ void attend_block(const uint32_t (&qa)[D / 16][4], fl
     for (int j = 0; j < 4; j++) {
       if constexpr (W == 4) {
         const uint4 v4 = *reinterpret_cast<const uint4*>(vt + T::off(toks[j], 16 * gid));
-        R[j][0] = v4.x ^ 0x80808080u;
-        R[j][1] = v4.y ^ 0x80808080u;
-        R[j][2] = v4.z ^ 0x80808080u;
-        R[j][3] = v4.w ^ 0x80808080u;
+        R[j][0] = v4.x;
+        R[j][1] = v4.y;
+        R[j][2] = v4.z;
+        R[j][3] = v4.w;
       } else {
         const uint2 v2 = *reinterpret_cast<const uint2*>(vt + T::off(toks[j], 8 * gid));
-        R[j][0] = v2.x ^ 0x80808080u;
-        R[j][1] = v2.y ^ 0x80808080u;
+        R[j][0] = v2.x;
+        R[j][1] = v2.y;
       }
     }
 #pragma unroll

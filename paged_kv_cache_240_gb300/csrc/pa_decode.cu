@@ -139,11 +139,12 @@ __device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2]
     for (int c = 0; c < D / 16; c += 2) {
       uint32_t r[4], a[4];
       ldsm_x4(r, kbase + T::off(krow, 16 * (c + (mi >> 1))));
-      biased_i8x4_to_f16_plus1152(r[0] ^ 0x80808080u, a[0], a[2]);  // tokens g,   step c
-      biased_i8x4_to_f16_plus1152(r[1] ^ 0x80808080u, a[1], a[3]);  // tokens g+8, step c
+      // the cache holds offset-binary bytes (code + 128): no sign fix-up
+      biased_i8x4_to_f16_plus1152(r[0], a[0], a[2]);  // tokens g,   step c
+      biased_i8x4_to_f16_plus1152(r[1], a[1], a[3]);  // tokens g+8, step c
       mma16816<false>(sa, a, qb[c][0], qb[c][1]);
-      biased_i8x4_to_f16_plus1152(r[2] ^ 0x80808080u, a[0], a[2]);  // step c+1
-      biased_i8x4_to_f16_plus1152(r[3] ^ 0x80808080u, a[1], a[3]);
+      biased_i8x4_to_f16_plus1152(r[2], a[0], a[2]);  // step c+1
+      biased_i8x4_to_f16_plus1152(r[3], a[1], a[3]);
       mma16816<false>(sb, a, qb[c + 1][0], qb[c + 1][1]);
     }
   }
@@ -274,7 +275,7 @@ __device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2]
       ldsm_x4_t(r, vbase + T::off(vrow, 32 * mp + 16 * (mi >> 1)));
 #pragma unroll
       for (int h = 0; h < 2; h++) {
-        const uint32_t x0 = r[2 * h] ^ 0x80808080u, x1 = r[2 * h + 1] ^ 0x80808080u;
+        const uint32_t x0 = r[2 * h], x1 = r[2 * h + 1];  // offset-binary code bytes
         uint32_t a[4];
         a[0] = __byte_perm(x0, 0x64646464u, 0x4240);  // row g:   tokens 2t, 2t+1
         a[1] = __byte_perm(x0, 0x64646464u, 0x4341);  // row g+8: tokens 2t, 2t+1

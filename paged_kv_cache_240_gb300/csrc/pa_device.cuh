@@ -244,8 +244,10 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // ------------------------------------------------------------------ int8 -> f16
 
 // The f16 with bit pattern 0x64XX is 1024 + XX exactly, so a code c in
-// [-128, 127] turned into the byte c + 128 (flip the top bit) and placed under
-// 0x64 is 1024 + 128 + c; subtracting 1152 leaves c exactly.  This is the
+// [-128, 127] turned into the byte c + 128 (flip the top bit: the form an int8
+// KV cache stores, while the weight codes of the linear layer are flipped as
+// they are loaded) and placed under 0x64 is 1024 + 128 + c; subtracting 1152
+// leaves c exactly.  This is the
 // published "magic number" integer-to-float conversion used by mixed-input
 // GEMMs (Kim et al., "Who Says Elephants Can't Run: Bringing Large Scale MoE
 // Models into Cloud Scale Production", 2022, Sec. 4), restated here.
@@ -255,7 +257,7 @@ __device__ __forceinline__ uint32_t f16x2_minus_1152(uint32_t biased) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Four codes (bytes 0..3 of w, already XOR-ed with 0x80808080) -> f16x2 pairs
+// Four codes (bytes 0..3 of w, each code + 128) -> f16x2 pairs
 // (c0, c1) and (c2, c3).
 __device__ __forceinline__ void biased_i8x4_to_f16(uint32_t u, uint32_t& lo, uint32_t& hi) {
   lo = f16x2_minus_1152(__byte_perm(u, 0x64646464u, 0x4140));

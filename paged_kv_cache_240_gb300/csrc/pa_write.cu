@@ -9,6 +9,8 @@
 // elements.  Bit-exactness with the CPU oracle rests on three facts: 16-bit ->
 // fp32 conversion is exact, fmaxf/fabsf are exact, and __fdiv_rn and
 // __float2int_rn are the IEEE round-to-nearest(-even) operations the oracle uses.
+// An int8 code c is stored as the byte c + 128 (offset binary), the form the
+// attention kernels turn into exact f16 operands without a sign fix-up.
 #include <type_traits>
 
 #include "pa_device.cuh"
@@ -67,7 +69,7 @@ __global__ void __launch_bounds__(kWriteWarps * 32) write_copy_kernel(WriteParam
 
 // Quantise one row held as E = D/32 consecutive elements per lane.
 template <int E>
-__device__ __forceinline__ void quantize_row(const float (&x)[E], int8_t (&q)[E], float& scale) {
+__device__ __forceinline__ void quantize_row(const float (&x)[E], uint8_t (&q)[E], float& scale) {
   float amax = 0.0f;
 #pragma unroll
   for (int e = 0; e < E; e++) amax = fmaxf(amax, fabsf(x[e]));
@@ -81,7 +83,7 @@ __device__ __forceinline__ void quantize_row(const float (&x)[E], int8_t (&q)[E]
       c = __float2int_rn(__fdiv_rn(x[e], scale));
       c = c > 127 ? 127 : (c < -127 ? -127 : c);
     }
-    q[e] = (int8_t)c;
+    q[e] = (uint8_t)(c + 128);  // stored offset binary
   }
 }
 
@@ -113,10 +115,10 @@ __global__ void __launch_bounds__(kWriteWarps * 32) write_quant_kernel(WritePara
     const IT* e = reinterpret_cast<const IT*>(&raw[which]);
 #pragma unroll
     for (int i = 0; i < E; i++) x[i] = in_to_f32<IT>(e[i]);
-    int8_t q[E];
+    uint8_t q[E];
     float scale;
     quantize_row<E>(x, q, scale);
-    int8_t* dst = reinterpret_cast<int8_t*>(which ? p.v_cache : p.k_cache) + dst_row * D + lane * E;
+    uint8_t* dst = (which ? p.v_cache : p.k_cache) + dst_row * D + lane * E;
     if constexpr (E == 4) {
       *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<uint32_t*>(q);
     } else {

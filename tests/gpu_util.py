@@ -10,7 +10,16 @@ from paged_kv_cache_240_gb300 import inputs as I
 ATOL, RTOL = 2e-3, 1e-2
 
 TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16}
-POISON_CODE = 0x55  # int8 code bytes of slots nothing wrote
+POISON_CODE = 0x55  # int8 cache bytes of slots nothing wrote (stored form)
+# An int8 cache stores each code c as the offset-binary byte c + 128 (include/pa.h);
+# the oracle keeps the codes themselves.  POISON_CODE as a stored byte stands for
+# this code:
+POISON_AS_CODE = int(np.uint8(POISON_CODE ^ 0x80).view(np.int8))  # as the oracle's int8
+
+
+def codes_of_stored(stored):
+    """Offset-binary cache bytes (numpy uint8/int8) -> the codes' bytes (uint8)."""
+    return stored.view(np.uint8) ^ np.uint8(0x80)
 
 
 def bits_to_torch(bits: np.ndarray, dtype: str, device="cuda"):
@@ -44,8 +53,8 @@ def poisoned_cache(w: I.Workload) -> pa.PagedCache:
 def oracle_poison(cache_o, dtype):
     """The same poison on the oracle's host cache, bit for bit."""
     if dtype == "i8":
-        cache_o.k[:] = POISON_CODE
-        cache_o.v[:] = POISON_CODE
+        cache_o.k[:] = POISON_AS_CODE
+        cache_o.v[:] = POISON_AS_CODE
         cache_o.k_scale[:] = np.float32(np.nan)
         cache_o.v_scale[:] = np.float32(np.nan)
     else:
@@ -69,10 +78,12 @@ def device_history(w: I.Workload, kh=None, vh=None):
 
 
 def cache_bits(cache: pa.PagedCache):
-    """Raw bytes of a device cache (K, V and scales) on the host."""
+    """Bytes of a device cache (K, V and scales) on the host, in the oracle's
+    form: an int8 cache's offset-binary bytes become the codes' bytes."""
     out = [cache.k.view(torch.int8).cpu().numpy().view(np.uint8),
            cache.v.view(torch.int8).cpu().numpy().view(np.uint8)]
     if cache.k_scale is not None:
+        out = [codes_of_stored(b) for b in out]
         out += [cache.k_scale.cpu().numpy().view(np.uint32),
                 cache.v_scale.cpu().numpy().view(np.uint32)]
     return out

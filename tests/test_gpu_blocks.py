@@ -10,7 +10,7 @@ import oracle
 import paged_kv_cache_240_gb300 as pa
 from paged_kv_cache_240_gb300 import inputs as I
 from paged_kv_cache_240_gb300.blocks import BlockManager
-from gpu_util import (POISON_CODE, TORCH_DT, assert_close, bits_to_torch, i32, new_err,
+from gpu_util import (POISON_AS_CODE, POISON_CODE, TORCH_DT, assert_close, bits_to_torch, i32, new_err,
                       oracle_poison)
 
 pytestmark = pytest.mark.gpu
@@ -56,7 +56,7 @@ def test_evicted_blocks_are_never_read(dtype, olib):
         else:
             cache.k[b].fill_(float("nan")), cache.v[b].fill_(float("nan"))
     if cache_dt == "i8":
-        cache_o.k[freed], cache_o.v[freed] = POISON_CODE, POISON_CODE
+        cache_o.k[freed], cache_o.v[freed] = POISON_AS_CODE, POISON_AS_CODE
         cache_o.k_scale[freed], cache_o.v_scale[freed] = np.float32(np.nan), np.float32(np.nan)
     else:
         nan = torch.full((1,), float("nan"), dtype=TORCH_DT[cache_dt]).view(torch.int16).item()

@@ -14,7 +14,8 @@ import oracle
 import oracle_checks as OC
 import paged_kv_cache_240_gb300 as pa
 from paged_kv_cache_240_gb300 import inputs as I
-from gpu_util import (assert_close, bits_to_torch, cache_bits, device_history, i32, new_err,
+from gpu_util import (assert_close, bits_to_torch, cache_bits, codes_of_stored, device_history,
+                      i32, new_err,
                       oracle_bits, oracle_poison, poisoned_cache, run_decode, run_prefill)
 
 pytestmark = pytest.mark.gpu
@@ -96,8 +97,9 @@ def test_write_golden_quant_cases():
                            i32([17]), err)
             torch.cuda.synchronize()
             assert cache.k_scale[1, 0, 1].item() == s and cache.v_scale[1, 0, 1].item() == s
-            assert (cache.k[1, 0, 1, :8].cpu().numpy() == c).all()
-            assert (cache.v[1, 0, 1, 8:].cpu().numpy() == 0).all()
+            # stored offset binary: byte = code + 128
+            assert (codes_of_stored(cache.k[1, 0, 1, :8].cpu().numpy()).view(np.int8) == c).all()
+            assert (codes_of_stored(cache.v[1, 0, 1, 8:].cpu().numpy()) == 0).all()
 
 
 def test_write_out_of_range_slot_flagged():
