@@ -107,17 +107,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return true;
 }
 
-// Bulk (non-tensor) copy global -> this CTA's shared memory; completion is
-// counted in bytes on `bar`.  dst, src and bytes are multiples of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // TMA tiled copy of the box at element coordinates (x, y) of a 2-D tensor map
 // into shared memory (dst aligned to the map's swizzle atom).  x * element size
 // is a multiple of 16 at every call site.
@@ -184,16 +173,6 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
-}
-
-// D = A(16x32 s8, row) * B(32x8 s8, col) + D with int32 accumulation (exact).
-__device__ __forceinline__ void imma16832(int (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                          uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // Transpose of an 8x8 b16 matrix held one row pair per thread (the layout
@@ -282,15 +261,6 @@ __device__ __forceinline__ void biased_i8x4_to_f16_plus1152(uint32_t u, uint32_t
                                                             uint32_t& hi) {
   lo = __byte_perm(u, 0x64646464u, 0x4140);
   hi = __byte_perm(u, 0x64646464u, 0x4342);
-}
-
-template <int K>
-__device__ __forceinline__ void biased_i8_pairs_plus1152(uint32_t a, uint32_t b, uint32_t& p0,
-                                                         uint32_t& p1) {
-  constexpr uint32_t sel = K == 0 ? 0x5140u : 0x7362u;
-  const uint32_t x = __byte_perm(a, b, sel);
-  p0 = __byte_perm(x, 0x64646464u, 0x4140);
-  p1 = __byte_perm(x, 0x64646464u, 0x4342);
 }
 
 // 2^x with the hardware approximation (relative error below 2^-22; -inf -> 0).
