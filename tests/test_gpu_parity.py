@@ -182,6 +182,66 @@ def test_decode_block_relabelling_bit_identical(pb, olib):
     assert (a == b).all()
 
 
+@pytest.mark.parametrize("name,kw,pb", [
+    ("qwen2.5-1.5b", dict(num_seqs=8, lens=("uniform", 1, 1500)), 0),
+    ("int8-kv", dict(num_seqs=5, lens=("uniform", 100, 900)), 2),
+    ("mha-7b", dict(num_seqs=3, lens=("uniform", 300, 700)), 1),
+])
+def test_decode_workspace_merge_scratch_and_reuse(name, kw, pb, olib):
+    """The workspace merge (partition states in the caller's scratch, merged by
+    a second kernel) needs no initialised workspace: scratch of all-ones bytes,
+    random bytes or arbitrary 64-bit words, then the same workspace reused by
+    repeated calls and by CUDA-graph replays, all give one result, bit for bit,
+    within the tolerance of the oracle."""
+    w = I.make_workload(name, seed=41, **kw)
+    cache_o, kh, vh = oracle_cache(olib, w)
+    cache, _ = device_history(w, kh, vh)
+    seqs = list(range(w.num_decode))
+    q_bits, ref = oracle_ref(olib, w, cache_o, seqs, 0.09)
+    q = bits_to_torch(q_bits, w.q_dtype)
+    tables, lens = i32(w.block_tables), i32(w.context_lens)
+    nbytes = pa.pa_decode_workspace_bytes(w.num_decode, w.num_q_heads, w.num_kv_heads,
+                                          w.head_dim, w.max_blocks_per_seq, w.window, pb)
+    assert nbytes > 0  # the batch takes the workspace merge
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    err = new_err()
+    out = torch.empty_like(q)
+
+    def call():
+        pa.pa_decode_partitioned(cache, out, q, tables, lens, 0.09, w.window, pb, ws, err)
+
+    rng = np.random.default_rng(5)
+    results = []
+    fills = [lambda: ws.fill_(0xFF),
+             lambda: ws.copy_(torch.from_numpy(rng.integers(0, 256, nbytes, dtype=np.uint8))),
+             # arbitrary 64-bit words
+             lambda: ws.view(torch.int64)[: nbytes // 8].copy_(torch.from_numpy(
+                 (rng.integers(1, 2 ** 39, nbytes // 8, dtype=np.int64) << 24)
+                 | rng.integers(1, 8, nbytes // 8, dtype=np.int64)))]
+    for fill in fills:
+        fill()
+        for _ in range(3):  # the same workspace, call after call
+            out.fill_(7.0)
+            call()
+            torch.cuda.synchronize()
+            results.append(out.double().cpu().numpy())
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            call()
+        for _ in range(3):  # replays repeat the captured launches
+            out.fill_(7.0)
+            g.replay()
+            torch.cuda.synchronize()
+            results.append(out.double().cpu().numpy())
+    assert int(err[0]) == 0
+    for r in results[1:]:
+        assert (r == results[0]).all()
+    assert_close(results[0], ref, "%s pb=%d" % (name, pb))
+
+
 @pytest.mark.parametrize("pb", [0, -3])
 def test_decode_empty_and_bad_data(pb, olib):
     """L = 0 gives zeros; a block id outside the pool drops its keys and sets
