@@ -309,7 +309,8 @@ def test_prefill_shapes(dtype, G, D, olib):
 
 def test_cuda_graph_replay_matches_direct_calls():
     """The calls only enqueue kernels on the caller's stream, so a CUDA graph of
-    a step (write + decode + prefill) replays to the same bits as direct calls."""
+    a step (write + decode + prefill) replays to the same bits as direct calls,
+    also with the prefill on a second stream running beside the decode."""
     w = I.make_workload("mixed", seed=31, num_seqs=5, num_chunks=2, chunk_len=70, window=300)
     kh, vh = I.history_rows(w)
     nd = w.num_decode
@@ -330,7 +331,7 @@ def test_cuda_graph_replay_matches_direct_calls():
                                           w.max_blocks_per_seq, w.window)
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
     outs = []
-    for use_graph in (False, True):
+    for use_graph, two_streams in ((False, False), (True, False), (True, True)):
         cache = poisoned_cache(w)
         err = new_err()
         hs = w.history_slot_mapping()[hist_mask]
@@ -339,11 +340,24 @@ def test_cuda_graph_replay_matches_direct_calls():
         o_dec, o_pre = torch.empty_like(q_dec), torch.empty_like(q_pre)
         stream = torch.cuda.Stream()
 
-        def step():
-            pa.pa_write_kv(cache, k_new, v_new, slots, err)
-            pa.pa_decode(cache, o_dec, q_dec, tables_dec, lens_dec, sm, w.window, ws, err)
+        side = torch.cuda.Stream()
+
+        def prefill():
             pa.pa_prefill_chunk(cache, o_pre, q_pre, cu, int(w.q_lens[nd:].max()), tables_pre,
                                 lens_pre, sm, w.window, err)
+
+        def step():
+            pa.pa_write_kv(cache, k_new, v_new, slots, err)
+            if two_streams:  # the prefill on a second stream, forked and joined in the graph
+                cur = torch.cuda.current_stream()
+                side.wait_stream(cur)
+                with torch.cuda.stream(side):
+                    prefill()
+                pa.pa_decode(cache, o_dec, q_dec, tables_dec, lens_dec, sm, w.window, ws, err)
+                cur.wait_stream(side)
+            else:
+                pa.pa_decode(cache, o_dec, q_dec, tables_dec, lens_dec, sm, w.window, ws, err)
+                prefill()
 
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
@@ -359,5 +373,6 @@ def test_cuda_graph_replay_matches_direct_calls():
         torch.cuda.synchronize()
         assert int(err[0]) == 0
         outs.append((o_dec.clone(), o_pre.clone()))
-    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
-    assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
+    for o in outs[1:]:
+        assert torch.equal(outs[0][0].view(torch.int16), o[0].view(torch.int16))
+        assert torch.equal(outs[0][1].view(torch.int16), o[1].view(torch.int16))

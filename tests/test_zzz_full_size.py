@@ -18,7 +18,9 @@ queries over L-C+j1 keys sees (query j sees keys up to L-C+j and the window
 behind it), so the oracle computes only those rows.
 
 Collected after every other test, so that a run stopping at the first failure
-has run the rest; each case builds a whole benchmark pool (up to ~3.5 GB)."""
+has run the rest; each case builds a whole benchmark pool (up to ~3.5 GB).  A step with both
+decoding sequences and prefill chunks runs its two attention calls as the
+benchmark does, the prefill on a second stream launched before the decode."""
 import pytest
 import torch
 
@@ -43,7 +45,7 @@ def test_full_size_step_sampled(name, olib):
     w = I.make_workload(name, seed=SEED)
     st = bench.DeviceStep(w, torch, pa, I, SEED)
     st.write()
-    st.attend()
+    st.attend(torch.cuda.Stream())
     torch.cuda.synchronize()
     assert int(st.err[0]) == 0
     assert check_sampled(st, w, SEED, olib) > 0
