@@ -215,6 +215,12 @@ class DeviceStep:
                                      self.tables_pre, self.lens_pre, self.sm, self.w.window,
                                      self.err)
 
+    def run(self, side=None):
+        """One step as the benchmark times it: the write, then the attention
+        calls (side by side when a second stream is given, see attend)."""
+        self.write()
+        self.attend(side)
+
     def attend(self, side=None):
         """The two attention calls.  Given a second stream ``side`` (and both calls
         having work), the prefill call is enqueued there first and the decode call
@@ -351,8 +357,7 @@ def time_ours(args, w, torch, pa, I, rank, world, steps=None, warmup=None):
     side = torch.cuda.Stream() if st.nd and st.max_q else None
 
     def step():
-        st.write()
-        st.attend(side)
+        st.run(side)
 
     if args.no_graph:
         run_step, run_dec, run_pre = step, st.decode, st.prefill

@@ -19,4 +19,6 @@ def test_readme_examples_run():
     torch.cuda.synchronize()
     assert ns["err"].item() == 0
     assert torch.isfinite(ns["out"].float()).all() and torch.isfinite(ns["outd"].float()).all()
+    assert torch.isfinite(ns["out_dec"].float()).all()
+    assert torch.isfinite(ns["out_pre"].float()).all()
     assert tuple(ns["y"].shape) == (8, 4096) and torch.isfinite(ns["y"].float()).all()

@@ -2,8 +2,8 @@
 
 Each pool is built exactly as the benchmark builds it (bench.DeviceStep: seeded
 device draws written through pa_write_kv in chunks of 32,768 history rows), one
-step runs (the new tokens' write, then pa_decode and pa_prefill_chunk), and the
-outputs of sampled sequences are recomputed by the oracle.  The oracle's inputs
+step runs (the new tokens' write and the attention calls), and the outputs of
+sampled sequences are recomputed by the oracle.  The oracle's inputs
 are the generator's draws for those sequences' rows, drawn again chunk by chunk,
 never what the kernels wrote: an int8 pool is quantised again by the oracle's own
 writer.  The oracle keeps block i of a sequence in its physical block i, where
@@ -18,9 +18,10 @@ queries over L-C+j1 keys sees (query j sees keys up to L-C+j and the window
 behind it), so the oracle computes only those rows.
 
 Collected after every other test, so that a run stopping at the first failure
-has run the rest; each case builds a whole benchmark pool (up to ~3.5 GB).  A step with both
-decoding sequences and prefill chunks runs its two attention calls as the
-benchmark does, the prefill on a second stream launched before the decode."""
+has run the rest; each case builds a whole benchmark pool (up to ~3.5 GB).  The step runs as the
+benchmark runs it (bench.DeviceStep.run): the write, then the attention calls;
+with both decoding sequences and prefill chunks, the prefill on a second stream
+launched before the decode."""
 import pytest
 import torch
 
@@ -44,8 +45,7 @@ def test_full_size_step_sampled(name, olib):
     _build.build()
     w = I.make_workload(name, seed=SEED)
     st = bench.DeviceStep(w, torch, pa, I, SEED)
-    st.write()
-    st.attend(torch.cuda.Stream())
+    st.run(torch.cuda.Stream())
     torch.cuda.synchronize()
     assert int(st.err[0]) == 0
     assert check_sampled(st, w, SEED, olib) > 0
