@@ -302,7 +302,7 @@ def roofline(w, dec_ms, pre_ms, peaks, src, full_size=True):
         achieved = decode_kv_bytes(w) / (dec_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name),
-                "kernel": "pa_decode (attention + split-K reduce)",
+                "kernel": "pa_decode (split-K attention and its merge)",
                 "peak_source": src + " hbm_gbs"}
     if not full_size:
         roof["traffic"] = None

@@ -140,7 +140,11 @@ pa_status pa_write_kv(const pa_cache *cache, const void *k, const void *v, pa_dt
  * the workspace and a second kernel merges them.  The partition size (64 blocks,
  * halved while the batch leaves SMs without two CTAs each) is chosen from the
  * batch shape and the device's SM count; the result does not depend on it
- * beyond rounding.  pa_decode_partitioned can instead merge inside the launch.
+ * beyond rounding.  A small batch whose block tables span at most 256 blocks and
+ * whose (sequence, kv head) pairs fill the SMs at 16 CTAs each is instead split
+ * into 16 partitions per sequence that merge inside the launch (a thread-block
+ * cluster; no workspace needed: pa_decode_workspace_bytes returns 0).
+ * pa_decode_partitioned chooses the partitioning explicitly.
  */
 pa_status pa_decode(const pa_cache *cache, void *out, const void *q, pa_dtype q_dtype,
                     int num_seqs, int num_q_heads, const int32_t *block_tables,

@@ -311,6 +311,10 @@ __device__ __forceinline__ int decode_parts(const AttnParams& p, int L, int& lo,
 // and refilled by one warp and no "stage empty" barrier is needed.
 constexpr int kDecWarps = 4;
 constexpr int kDecThreads = kDecWarps * 32;
+// Cluster merge: at most 16 CTAs per cluster (the non-portable maximum, checked
+// on the device).
+constexpr int kMaxCluster = 16;
+static_assert(kMaxCluster * kDecHeads <= kDecThreads, "one thread per (partition, row)");
 static_assert(kStages == 2 * kDecWarps, "two stages per decode warp");
 
 template <int MODE, int D>
@@ -322,7 +326,11 @@ struct DecSmem {
   static constexpr int kPartOff = (kMergeBytes + 127) / 128 * 128;
   static constexpr int kPartOOff = kPartOff + (2 * kDecHeads + 4) * 4;
   static constexpr int kPartBytes = kPartOOff - kPartOff + kDecHeads * D * 4;
-  static_assert(kPartOff + kPartBytes <= Smem<MODE, D>::kDataBytes,
+  // then, private to this CTA, the partitions' states gathered for the merge:
+  // m (then weights) [16][8], l [16][8], the rows' maxima [8] and 1 / normaliser [8]
+  static constexpr int kGatherOff = kPartOff + kPartBytes;
+  static constexpr int kGatherBytes = (2 * kMaxCluster * kDecHeads + 2 * kDecHeads) * 4;
+  static_assert(kGatherOff + kGatherBytes <= Smem<MODE, D>::kDataBytes,
                 "merge areas must fit the stages");
 };
 
@@ -571,25 +579,52 @@ __global__ void __launch_bounds__(kDecThreads, MODE == kI8 ? 5 : 3)
     // the cluster rank is the partition (grid x = partition + num_parts * ...)
     if (threadIdx.x == 0) *pok = (!aborted && cluster_ctarank() == (uint32_t)part) ? 1 : 0;
     cluster_sync_all();  // every partition's state is in place
-    bool all_ok = true;
-    for (int q = 0; q < nparts; q++)
-      all_ok = all_ok && __float_as_int(ld_cluster_f32(pok, q)) == 1;
+    // No remote read below waits for another: each partition's (m, l) of every
+    // row and its flag, one thread per (partition, row), into this CTA's shared
+    // memory; the rows' maxima, normalisers and the partitions' weights there;
+    // then each output element's partition outputs, all issued at once.
+    float* gm = reinterpret_cast<float*>(s.stages + DS::kGatherOff);  // [q][8]: m, then weight
+    float* gl = gm + kMaxCluster * kDecHeads;                          // [q][8]: l
+    float* rmax = gl + kMaxCluster * kDecHeads;                        // [8]
+    float* rinv = rmax + kDecHeads;                                    // [8]: 1 / normaliser
+    bool ok_q = true;
+    if (threadIdx.x < nparts * kDecHeads) {
+      const int q = threadIdx.x / kDecHeads, r = threadIdx.x % kDecHeads;
+      gm[threadIdx.x] = r < rows ? ld_cluster_f32(pm + r, q) : -INFINITY;
+      gl[threadIdx.x] = r < rows ? ld_cluster_f32(pl + r, q) : 0.0f;
+      if (r == 0) ok_q = __float_as_int(ld_cluster_f32(pok, q)) == 1;
+    }
+    const bool all_ok = __syncthreads_and(ok_q) != 0;
+    if (threadIdx.x < rows) {
+      const int r = threadIdx.x;
+      float M = -INFINITY;
+      for (int q = 0; q < nparts; q++) M = fmaxf(M, gm[q * kDecHeads + r]);
+      float den = 0.0f;
+      if (M != -INFINITY)
+        for (int q = 0; q < nparts; q++)
+          den += exp2f(gm[q * kDecHeads + r] - M) * gl[q * kDecHeads + r];
+      rmax[r] = M;
+      rinv[r] = den > 0.0f ? 1.0f / den : 0.0f;
+    }
+    __syncthreads();
+    if (threadIdx.x < nparts * kDecHeads) {  // weight 2^(m_q - M); 0 without a key
+      const float M = rmax[threadIdx.x % kDecHeads];
+      gm[threadIdx.x] = M != -INFINITY ? exp2f(gm[threadIdx.x] - M) : 0.0f;
+    }
+    __syncthreads();
     if (all_ok) {
       for (int idx = part * kDecThreads + threadIdx.x; idx < rows * D;
            idx += p.num_parts * kDecThreads) {
         const int r = idx / D, d = idx % D;
-        float M = -INFINITY;
-        for (int q = 0; q < nparts; q++) M = fmaxf(M, ld_cluster_f32(pm + r, q));
-        float num = 0.0f, den = 0.0f;
-        if (M != -INFINITY) {
-          for (int q = 0; q < nparts; q++) {
-            const float e = exp2f(ld_cluster_f32(pm + r, q) - M);
-            num += e * ld_cluster_f32(po + r * D + d, q);
-            den += e * ld_cluster_f32(pl + r, q);
-          }
-        }
-        out[((long long)b * p.num_q_heads + h0 + r) * D + d] =
-            to_out<QT>(den > 0.0f ? num / den : 0.0f);
+        float v[kMaxCluster];
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; q++)
+          v[q] = q < nparts ? ld_cluster_f32(po + r * D + d, q) : 0.0f;
+        float num = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; q++)
+          if (q < nparts) num += gm[q * kDecHeads + r] * v[q];
+        out[((long long)b * p.num_q_heads + h0 + r) * D + d] = to_out<QT>(num * rinv[r]);
       }
     }
     cluster_sync_all();  // no CTA leaves while another still reads its state
@@ -721,9 +756,6 @@ int max_blocks_touched(int max_blocks_per_seq, int window) {
   return std::min(max_blocks_per_seq, (window + 2 * kBlock - 2) / kBlock);
 }
 
-// Cluster merge: at most 16 CTAs per cluster (the non-portable maximum, checked
-// on the device).
-constexpr int kMaxCluster = 16;
 
 // Whether a cluster of `size` decode CTAs with the largest shared-memory
 // footprint (16-bit cache, head_dim 128) can be resident on the current device;
@@ -792,19 +824,34 @@ Split workspace_split(long long units, int maxb, int partition_blocks, int sms) 
 // partition_blocks > 0: fixed partitions, workspace merge.  partition_blocks < 0:
 // each sequence split evenly into up to -partition_blocks partitions (at most 16),
 // cluster merge (a cluster the device cannot hold falls back to the workspace
-// merge).  0: the workspace merge with 64-block partitions, halved while the
-// batch gives the SMs fewer than two CTAs each.  Measured on GB300, the cluster
-// merge was never faster on the benchmark batches: evenly split clusters cost
-// every sequence P CTAs' fixed work (7B MHA, INT8 and mixed batches 1-18 %
-// slower), and on the Qwen2.5-1.5B batch, whose step is latency-bound, 16-CTA
-// clusters took 17.3 us against 16.9 us with the merge kernel.
+// merge).  0, the automatic choice: the workspace merge with 64-block partitions
+// while the batch gives every SM two CTAs that way; a smaller batch whose
+// sequences span at most 256 blocks and whose (sequence, kv head, row group)
+// units fill the SMs at 16 CTAs each takes 16-CTA clusters (each CTA at most
+// 16 blocks, no merge launch); a smaller one still halves the workspace
+// partitions (down to 4 blocks).  Measured on GB300 (decode call, graph
+// replays, L2 flushed): the Qwen2.5-1.5B batch 15.2 us with 16-CTA clusters
+// against 17.0 us with the merge kernel; the 7B MHA, INT8 and mixed batches
+// keep the workspace merge (clusters of 2-16 measured 1 % faster to 2x slower).
 Split choose_split(int num_seqs, int num_kv_heads, int row_groups, int max_blocks_per_seq,
                    int window, int partition_blocks) {
   const int maxb = max_blocks_touched(max_blocks_per_seq, window);
   const long long units = (long long)num_seqs * num_kv_heads * row_groups;
   const int sms = std::max(current_sm_count(), 1);
   if (partition_blocks > 0) return workspace_split(units, maxb, partition_blocks, sms);
-  if (partition_blocks == 0) return workspace_split(units, maxb, 0, sms);
+  if (partition_blocks == 0) {
+    const bool small = units * ((maxb + 63) / 64) < 2LL * sms;
+    if (small && maxb > kMaxCluster && maxb <= kMaxCluster * kMaxCluster &&
+        units * kMaxCluster >= sms && cluster_fits(kMaxCluster)) {
+      Split s;
+      s.mode = kMergeCluster;
+      s.part_blocks = 0;
+      s.num_parts = kMaxCluster;
+      s.min_part_blocks = 1;
+      return s;
+    }
+    return workspace_split(units, maxb, 0, sms);
+  }
   int P = std::min(std::min(-partition_blocks, kMaxCluster), maxb);
   const int min_part = 1;
   P = std::max(P, 1);

@@ -183,8 +183,8 @@ def test_decode_block_relabelling_bit_identical(pb, olib):
 
 
 @pytest.mark.parametrize("name,kw,pb", [
-    ("qwen2.5-1.5b", dict(num_seqs=8, lens=("uniform", 1, 1500)), 0),
-    ("int8-kv", dict(num_seqs=5, lens=("uniform", 100, 900)), 2),
+    ("qwen2.5-1.5b", dict(num_seqs=8, lens=("uniform", 1, 1500)), 8),
+    ("int8-kv", dict(num_seqs=5, lens=("uniform", 100, 900)), 0),
     ("mha-7b", dict(num_seqs=3, lens=("uniform", 300, 700)), 1),
 ])
 def test_decode_workspace_merge_scratch_and_reuse(name, kw, pb, olib):
