@@ -140,6 +140,25 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ device workload
 
+def pack_tensors(torch, tensors, dev):
+    """One uint8 device buffer holding the tensors back to back, each at a
+    256-byte boundary (the library wants 16), and views of it shaped and typed
+    like them with their values copied in: a step's inputs (or outputs) then move
+    between host and device in one copy."""
+    sizes = [t.numel() * t.element_size() for t in tensors]
+    offs, off = [], 0
+    for nb in sizes:
+        offs.append(off)
+        off += (nb + 255) // 256 * 256
+    buf = torch.empty(max(off, 256), dtype=torch.uint8, device=dev)
+    views = []
+    for t, o, nb in zip(tensors, offs, sizes):
+        v = buf[o:o + nb].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        views.append(v)
+    return buf, views
+
+
 class DeviceStep:
     """Everything one step needs, resident on the device ``dev`` (the host serves only
     checks of this bookkeeping that stand host functions in for the library's calls)."""
@@ -186,6 +205,10 @@ class DeviceStep:
                                               w.max_blocks_per_seq, w.window)
         self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
         self.reduce_launched = nbytes > 0 and nd > 0
+        # the step's inputs, and its outputs, each packed into one device buffer so
+        # that the end-to-end run moves them with one copy each way
+        self.inputs_buf = self._pack(self.INPUTS, dev)
+        self.outputs_buf = self._pack(self.OUTPUTS, dev)
         if torch.device(dev).type == "cuda":
             torch.cuda.synchronize()
         if int(self.err[0]) != 0:
@@ -195,6 +218,13 @@ class DeviceStep:
     INPUTS = ("q_dec", "q_pre", "k_new", "v_new", "slots", "tables_dec", "tables_pre",
               "lens_dec", "lens_pre", "cu")
     OUTPUTS = ("out_dec", "out_pre")
+
+    def _pack(self, names, dev):
+        """Pack the named tensors into one buffer (pack_tensors); they become its views."""
+        buf, views = pack_tensors(self.torch, [getattr(self, n) for n in names], dev)
+        for n, v in zip(names, views):
+            setattr(self, n, v)
+        return buf
 
     def launches_per_step(self):
         n = 1 + (1 if self.nd else 0) + (1 if self.reduce_launched else 0)
@@ -404,22 +434,20 @@ def time_ours(args, w, torch, pa, I, rank, world, steps=None, warmup=None):
         if int(st.err[0]) != 0:
             raise RuntimeError("device flags %d during the timed steps" % int(st.err[0]))
 
-        # end to end: the step's inputs from pinned host memory, its output back
-        host = {name: getattr(st, name).cpu().pin_memory() for name in st.INPUTS}
-        outs = {name: torch.empty(getattr(st, name).shape, dtype=getattr(st, name).dtype
-                                  ).pin_memory() for name in st.OUTPUTS}
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = sum(t.numel() * t.element_size() for t in outs.values())
+        # end to end: the step's inputs from pinned host memory, its outputs back,
+        # each direction one copy of the packed buffer
+        host_in = st.inputs_buf.cpu().pin_memory()
+        host_out = torch.empty(st.outputs_buf.shape, dtype=torch.uint8).pin_memory()
+        h2d = host_in.numel()
+        d2h = host_out.numel()
         e2e_steps = max(3, min(steps, 200))
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         s0.record(stream)
         for _ in range(e2e_steps):
-            for name, t in host.items():
-                getattr(st, name).copy_(t, non_blocking=True)
+            st.inputs_buf.copy_(host_in, non_blocking=True)
             run_step()
-            for name, t in outs.items():
-                t.copy_(getattr(st, name), non_blocking=True)
+            host_out.copy_(st.outputs_buf, non_blocking=True)
         s1.record(stream)
         torch.cuda.synchronize()
     e2e_ms = s0.elapsed_time(s1) / e2e_steps
@@ -653,6 +681,13 @@ def bench_linear(args):
     build()
     from paged_kv_cache_240_gb300 import linear as L
     layers_dev = linear_layers(torch, groups, m, args.seed + 1000 * rank)
+    # every group's activations in one device buffer, every output in another, so
+    # that the end-to-end run moves each direction in one copy
+    x_buf, xs = pack_tensors(torch, [x for x, _ in layers_dev], "cuda")
+    y_buf, ys = pack_tensors(torch, [y for _, mats in layers_dev for _, _, y in mats], "cuda")
+    it = iter(ys)
+    layers_dev = [(x, [(c, sc, next(it)) for c, sc, _ in mats])
+                  for x, (_, mats) in zip(xs, layers_dev)]
     launches = len(groups)  # one grouped launch per group, splits merged in the launch
     stream = torch.cuda.Stream()
 
@@ -680,22 +715,19 @@ def bench_linear(args):
         if world > 1:
             torch.distributed.barrier()
         clk = clocks.stop()
-        # end to end: every group's activations in from pinned memory, outputs back
-        hx = [x.cpu().pin_memory() for x, _ in layers_dev]
-        ys = [y for _, mats in layers_dev for _, _, y in mats]
-        hy = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys]
-        h2d = sum(t.numel() * t.element_size() for t in hx)
-        d2h = sum(t.numel() * t.element_size() for t in hy)
+        # end to end: every group's activations in from pinned memory, the outputs
+        # back, each direction one copy of the packed buffer
+        hx = x_buf.cpu().pin_memory()
+        hy = torch.empty(y_buf.shape, dtype=torch.uint8).pin_memory()
+        h2d, d2h = hx.numel(), hy.numel()
         e2e_steps = max(3, min(args.steps, 100))
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         s0.record(stream)
         for _ in range(e2e_steps):
-            for (x, _), t in zip(layers_dev, hx):
-                x.copy_(t, non_blocking=True)
+            x_buf.copy_(hx, non_blocking=True)
             run()
-            for y, t in zip(ys, hy):
-                t.copy_(y, non_blocking=True)
+            hy.copy_(y_buf, non_blocking=True)
         s1.record(stream)
         torch.cuda.synchronize()
     total_ms, e2e_ms = max_over_ranks(torch, [sum(step_ms), s0.elapsed_time(s1) / e2e_steps],
