@@ -227,6 +227,8 @@ class DeviceStep:
         return buf
 
     def launches_per_step(self):
+        if self.nd and not self.max_q:  # pa_decode_append (+ its merge kernel)
+            return 1 + (1 if self.reduce_launched else 0)
         n = 1 + (1 if self.nd else 0) + (1 if self.reduce_launched else 0)
         return n + (1 if self.max_q else 0)
 
@@ -246,8 +248,15 @@ class DeviceStep:
                                      self.err)
 
     def run(self, side=None):
-        """One step as the benchmark times it: the write, then the attention
-        calls (side by side when a second stream is given, see attend)."""
+        """One step as the benchmark times it: decoding sequences alone in one
+        launch (pa_decode_append: each new token written at its position, then
+        the attention); otherwise the write, then the attention calls (side by
+        side when a second stream is given, see attend)."""
+        if self.nd and not self.max_q:
+            self.pa.pa_decode_append(self.cache, self.k_new, self.v_new, self.out_dec, self.q_dec,
+                                     self.tables_dec, self.lens_dec, self.sm, self.w.window,
+                                     self.ws, self.err)
+            return
         self.write()
         self.attend(side)
 

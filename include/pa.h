@@ -172,6 +172,34 @@ pa_status pa_decode_partitioned(const pa_cache *cache, void *out, const void *q,
                                 size_t workspace_bytes, int32_t *err_flag, void *stream);
 
 /*
+ * pa_decode_append -- one decode step in one launch: each sequence's new token
+ * is written at its position context_lens[b] - 1, the slot its block table
+ * names there, and then the batch attends as pa_decode ("PyTorch LLM Serving
+ * Engine", "Loading": the new K/V goes to its physical slot and the query
+ * attends to the whole context, itself included).  The same results, bit for
+ * bit, as pa_write_kv of those slots followed by pa_decode.
+ *
+ *   k_new, v_new  [num_seqs][num_kv_heads][head_dim] of kv_dtype: a 16-bit cache
+ *                 takes its own type (copied); an int8 cache quantises them as
+ *                 pa_write_kv does.  kv_dtype must equal q_dtype.
+ *   the rest      as pa_decode (its automatic partitioning and workspace size)
+ *
+ * The warp that copies the block holding position context_lens[b] - 1 writes
+ * the row first.  A sequence with context_lens[b] = 0 writes nothing; one whose
+ * block id at that position is outside the pool writes nothing and sets
+ * PA_FLAG_BLOCK_ID, as the attention does.  A step whose new tokens go
+ * elsewhere than position context_lens[b] - 1 needs pa_write_kv + pa_decode.
+ * Errors: pa_decode's, plus PA_ERR_INVALID_ARG for a NULL or misaligned k_new or
+ * v_new and PA_ERR_UNSUPPORTED for kv_dtype != q_dtype.
+ */
+pa_status pa_decode_append(const pa_cache *cache, const void *k_new, const void *v_new,
+                           pa_dtype kv_dtype, void *out, const void *q, pa_dtype q_dtype,
+                           int num_seqs, int num_q_heads, const int32_t *block_tables,
+                           int max_blocks_per_seq, const int32_t *context_lens, float sm_scale,
+                           int window, void *workspace, size_t workspace_bytes,
+                           int32_t *err_flag, void *stream);
+
+/*
  * Workspace bytes pa_decode / pa_decode_partitioned need for these arguments
  * (partition_blocks as for pa_decode_partitioned; 0 = the automatic choice,
  * evaluated on the current device).  Returns 0 when no workspace is needed (a

@@ -16,7 +16,7 @@ import os
 __all__ = [
     "PaError", "PagedCache", "load_library", "pa_write_kv", "pa_decode",
     "pa_decode_partitioned", "pa_decode_workspace_bytes", "pa_decode_noalloc",
-    "pa_prefill_chunk",
+    "pa_decode_append", "pa_prefill_chunk",
     "pa_status_str", "pa_check_flags", "PA_FLAG_SLOT_RANGE", "PA_FLAG_BLOCK_ID",
     "PA_FLAG_CONTEXT_LEN", "PA_FLAG_Q_LEN", "PA_FLAG_TIMEOUT", "EXPORTED_SYMBOLS",
     "pa_last_cuda_error", "pa_selftest_bounded_wait",
@@ -31,7 +31,8 @@ PA_FLAG_SLOT_RANGE, PA_FLAG_BLOCK_ID, PA_FLAG_CONTEXT_LEN, PA_FLAG_Q_LEN, PA_FLA
     1, 2, 4, 8, 16)
 
 EXPORTED_SYMBOLS = ("pa_write_kv", "pa_decode", "pa_decode_partitioned",
-                    "pa_decode_workspace_bytes", "pa_decode_noalloc", "pa_prefill_chunk",
+                    "pa_decode_workspace_bytes", "pa_decode_noalloc", "pa_decode_append",
+                    "pa_prefill_chunk",
                     "pa_status_str", "pa_last_cuda_error", "pa_check_flags",
                     "pa_blocks_create", "pa_blocks_destroy", "pa_blocks_append",
                     "pa_blocks_rollback", "pa_blocks_release", "pa_blocks_preempt",
@@ -83,8 +84,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_last_cuda_error.argtypes = []
     lib.pa_last_cuda_error.restype = ctypes.c_char_p
     lib.pa_selftest_bounded_wait.argtypes = [ctypes.c_longlong, P, P, P]
+    lib.pa_decode_append.argtypes = [cp, P, P, I, P, P, I, I, I, P, I, P, F, I, P, S, P, P]
     for name in ("pa_write_kv", "pa_decode", "pa_decode_partitioned", "pa_decode_noalloc",
-                 "pa_prefill_chunk", "pa_check_flags", "pa_selftest_bounded_wait"):
+                 "pa_decode_append", "pa_prefill_chunk", "pa_check_flags",
+                 "pa_selftest_bounded_wait"):
         getattr(lib, name).restype = I
     if path == LIB_PATH:
         _lib = lib
@@ -236,6 +239,21 @@ def pa_decode(cache: PagedCache, out, q, block_tables, context_lens, sm_scale, w
         ctypes.byref(st), _ptr(out), _ptr(q), _dtype_code(q), int(q.shape[0]), int(q.shape[1]),
         _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), float(sm_scale),
         int(window), _ptr(workspace), nbytes, _ptr(err_flag), _stream(stream)), "pa_decode")
+
+
+def pa_decode_append(cache: PagedCache, k_new, v_new, out, q, block_tables, context_lens,
+                     sm_scale, window, workspace, err_flag, stream=None):
+    """One decode step in one launch: k_new, v_new [B, Hkv, D] written at each
+    sequence's position context_lens[b] - 1, then q, out [B, Hq, D] attend; the
+    same bits as pa_write_kv of those slots followed by pa_decode."""
+    _check_cuda(k_new, v_new, out, q, block_tables, context_lens, workspace, err_flag)
+    st = cache.struct()
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _raise(load_library().pa_decode_append(
+        ctypes.byref(st), _ptr(k_new), _ptr(v_new), _dtype_code(k_new), _ptr(out), _ptr(q),
+        _dtype_code(q), int(q.shape[0]), int(q.shape[1]), _ptr(block_tables),
+        int(block_tables.shape[1]), _ptr(context_lens), float(sm_scale), int(window),
+        _ptr(workspace), nbytes, _ptr(err_flag), _stream(stream)), "pa_decode_append")
 
 
 def pa_decode_noalloc(cache: PagedCache, out, q, block_tables, context_lens, sm_scale, window,

@@ -58,6 +58,10 @@ struct AttnParams {
   // kMergeCluster: each sequence's blocks split evenly into at most num_parts
   // partitions of at least min_part_blocks, merged inside the launch)
   int merge_mode, min_part_blocks;
+  // decode: the step's new rows [num_seqs][num_kv_heads][D] (q's type) to write
+  // at each sequence's position L-1 before attending, or null
+  const void* k_new;
+  const void* v_new;
 };
 constexpr int kMergeWorkspace = 0, kMergeCluster = 1;
 

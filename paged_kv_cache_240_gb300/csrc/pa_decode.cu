@@ -27,6 +27,7 @@
 // the result is bit-identical under any relabelling of physical blocks.
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "pa_attn_common.cuh"
 #include "pa_internal.h"
@@ -287,6 +288,42 @@ __device__ __forceinline__ void attend_block_dec(const uint32_t (&qb)[D / 16][2]
   }
 }
 
+// The step's new K and V rows of (sequence b, kv head kvh) written into slot
+// `off` of physical block `phys` by one warp (E = D/32 elements per lane; an
+// int8 cache quantises them as the KV write does), then ordered before the TMA
+// copy of that block (generic-proxy writes, then an async-proxy read).
+template <int MODE, int D, typename QT>
+__device__ __forceinline__ void write_new_row(const AttnParams& p, int b, int kvh, int phys,
+                                              int off, int lane) {
+  constexpr int E = D / 32;
+  using R = typename std::conditional<E == 4, uint2, uint32_t>::type;  // E 16-bit values
+  const long long src = ((long long)b * p.num_kv_heads + kvh) * D + lane * E;
+  const long long dst_row = ((long long)phys * p.num_kv_heads + kvh) * kBlock + off;
+#pragma unroll
+  for (int which = 0; which < 2; which++) {
+    const R raw = *reinterpret_cast<const R*>(static_cast<const QT*>(which ? p.v_new : p.k_new) +
+                                              src);
+    uint8_t* cache = const_cast<uint8_t*>(which ? p.v_cache : p.k_cache);
+    if constexpr (MODE == kI8) {
+      float x[E];
+      const QT* e = reinterpret_cast<const QT*>(&raw);
+#pragma unroll
+      for (int i = 0; i < E; i++) x[i] = in_to_f32<QT>(e[i]);
+      uint8_t q[E];
+      float scale;
+      quantize_row<E>(x, q, scale);
+      uint8_t* dst = cache + dst_row * D + lane * E;
+      if constexpr (E == 4) *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<uint32_t*>(q);
+      else *reinterpret_cast<uint16_t*>(dst) = *reinterpret_cast<uint16_t*>(q);
+      if (lane == 0) const_cast<float*>(which ? p.v_scale : p.k_scale)[dst_row] = scale;
+    } else {
+      *reinterpret_cast<R*>(cache + (dst_row * D + lane * E) * 2) = raw;
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __syncwarp();
+}
+
 // Partitions of a sequence with visible context L, their size in blocks (psz)
 // and the visible range (keys from lo, blocks first..last).  L >= 1.
 __device__ __forceinline__ int decode_parts(const AttnParams& p, int L, int& lo, int& first,
@@ -398,7 +435,10 @@ __device__ __forceinline__ void fetch_block(const AttnParams& p, const void* tmk
   }
 }
 
-template <int MODE, int D, typename QT>
+// WRITE: the launch also writes the step's new rows (p.k_new, p.v_new) at each
+// sequence's position L-1 (an instance of its own, so that the plain decode's
+// register allocation does not carry the write).
+template <int MODE, int D, typename QT, bool WRITE>
 __global__ void __launch_bounds__(kDecThreads, MODE == kI8 ? 5 : 3)
     pa_decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv) {
@@ -437,11 +477,23 @@ __global__ void __launch_bounds__(kDecThreads, MODE == kI8 ? 5 : 3)
   // block ids of this warp's blocks k = 0..nmine-1 (logical block blk0 + warp + 4k)
   const int32_t* table = p.block_tables + (long long)b * p.max_blocks_per_seq + blk0 + warp;
   int ids = lane < nmine ? table[kDecWarps * lane] : -1;
+  // with the step's new rows given, the warp that copies the block holding
+  // position L-1 writes them into it first (before its first copy, so that the
+  // write's registers are free again in the loop)
+  if constexpr (WRITE) {
+    const int j = last - blk0;  // the newest block's index in this partition
+    if (j >= 0 && j < nblk && j % kDecWarps == warp) {
+      const int phys = p.block_tables[(long long)b * p.max_blocks_per_seq + last];
+      if (phys >= 0 && phys < p.num_blocks)
+        write_new_row<MODE, D, QT>(p, b, kvh, phys, (L - 1) % kBlock, lane);
+    }
+  }
+  auto fetch = [&](int k, int slot, int phys) {
+    fetch_block<MODE, D>(p, &tmk, &tmv, s, slot, phys, kvh, lane);
+  };
 #pragma unroll
   for (int k = 0; k < 2; k++)
-    if (k < nmine)
-      fetch_block<MODE, D>(p, &tmk, &tmv, s, warp + kDecWarps * k,
-                           __shfl_sync(0xffffffffu, ids, k), kvh, lane);
+    if (k < nmine) fetch(k, warp + kDecWarps * k, __shfl_sync(0xffffffffu, ids, k));
 
   const int g = lane >> 2, t = lane & 3;
   const QT* q = static_cast<const QT*>(p.q);
@@ -496,8 +548,7 @@ __global__ void __launch_bounds__(kDecThreads, MODE == kI8 ? 5 : 3)
     if (k + 2 < nmine) {
       if (((k + 2) & 31) == 0)  // next 32 of this warp's block ids
         ids = (k + 2 + lane) < nmine ? table[kDecWarps * (k + 2 + lane)] : -1;
-      fetch_block<MODE, D>(p, &tmk, &tmv, s, slot, __shfl_sync(0xffffffffu, ids, (k + 2) & 31),
-                           kvh, lane);
+      fetch(k + 2, slot, __shfl_sync(0xffffffffu, ids, (k + 2) & 31));
     }
   }
   if (kfail >= 0) {  // no copy may still be landing in shared memory when the CTA exits
@@ -769,7 +820,7 @@ bool cluster_fits(int size) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   std::lock_guard<std::mutex> lock(mu);
   if (known[dev][size] == 0) {
-    auto kern = pa_decode_kernel<kF16, 128, __half>;
+    auto kern = pa_decode_kernel<kF16, 128, __half, false>;
     constexpr int smem = Smem<kF16, 128>::kBytes;
     bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
                   cudaSuccess &&
@@ -875,7 +926,7 @@ template <int MODE, int D, typename QT>
 cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
                           int num_seqs, cudaStream_t stream) {
   constexpr int smem = Smem<MODE, D>::kBytes;
-  auto kern = pa_decode_kernel<MODE, D, QT>;
+  auto kern = p.k_new ? pa_decode_kernel<MODE, D, QT, true> : pa_decode_kernel<MODE, D, QT, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(p.num_parts * p.num_kv_heads * p.row_groups), (unsigned)num_seqs);
@@ -916,13 +967,16 @@ extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int n
   return workspace_for(num_seqs, num_q_heads, head_dim, s);
 }
 
-extern "C" pa_status pa_decode_partitioned(const pa_cache* cache, void* out, const void* q,
-                                           pa_dtype q_dtype, int num_seqs, int num_q_heads,
-                                           const int32_t* block_tables, int max_blocks_per_seq,
-                                           const int32_t* context_lens, float sm_scale, int window,
-                                           int partition_blocks, void* workspace,
-                                           size_t workspace_bytes, int32_t* err_flag,
-                                           void* stream) {
+namespace {
+
+// pa_decode_partitioned, and with k_new / v_new (of kv_dtype) the write of the
+// step's new rows in the same launch (pa_decode_append).
+pa_status decode_call(const pa_cache* cache, void* out, const void* q, pa_dtype q_dtype,
+                      int num_seqs, int num_q_heads, const int32_t* block_tables,
+                      int max_blocks_per_seq, const int32_t* context_lens, float sm_scale,
+                      int window, int partition_blocks, void* workspace, size_t workspace_bytes,
+                      int32_t* err_flag, void* stream, const void* k_new, const void* v_new,
+                      pa_dtype kv_dtype) {
   using pa_internal::aligned16;
   pa_status st = pa_internal::check_cache(cache);
   if (st != PA_OK) return st;
@@ -939,6 +993,10 @@ extern "C" pa_status pa_decode_partitioned(const pa_cache* cache, void* out, con
     if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
   } else if (q_dtype != cache->dtype) {
     return PA_ERR_UNSUPPORTED;
+  }
+  if (k_new || v_new) {  // the step's new rows: q's 16-bit type, 16-byte aligned
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return PA_ERR_INVALID_ARG;
+    if (kv_dtype != q_dtype) return PA_ERR_UNSUPPORTED;
   }
   if (num_seqs > 65535 || !pa_internal::cache_rows_fit(cache)) return PA_ERR_UNSUPPORTED;
   if ((long long)max_blocks_per_seq * kBlock > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
@@ -975,6 +1033,8 @@ extern "C" pa_status pa_decode_partitioned(const pa_cache* cache, void* out, con
   p.merge_mode = sp.mode;
   p.min_part_blocks = sp.min_part_blocks;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.k_new = k_new;
+  p.v_new = v_new;
   if (need > 0) {
     const size_t n = (size_t)num_seqs * num_q_heads * sp.num_parts;
     p.ws_o = static_cast<float*>(workspace);
@@ -994,6 +1054,33 @@ extern "C" pa_status pa_decode_partitioned(const pa_cache* cache, void* out, con
   else if (q_dtype == PA_F16) e = launch_decode_d<kI8, __half>(p, tmk, tmv, D, num_seqs, s);
   else e = launch_decode_d<kI8, __nv_bfloat16>(p, tmk, tmv, D, num_seqs, s);
   return pa_internal::cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" pa_status pa_decode_partitioned(const pa_cache* cache, void* out, const void* q,
+                                           pa_dtype q_dtype, int num_seqs, int num_q_heads,
+                                           const int32_t* block_tables, int max_blocks_per_seq,
+                                           const int32_t* context_lens, float sm_scale, int window,
+                                           int partition_blocks, void* workspace,
+                                           size_t workspace_bytes, int32_t* err_flag,
+                                           void* stream) {
+  return decode_call(cache, out, q, q_dtype, num_seqs, num_q_heads, block_tables,
+                     max_blocks_per_seq, context_lens, sm_scale, window, partition_blocks,
+                     workspace, workspace_bytes, err_flag, stream, nullptr, nullptr, q_dtype);
+}
+
+extern "C" pa_status pa_decode_append(const pa_cache* cache, const void* k_new,
+                                      const void* v_new, pa_dtype kv_dtype, void* out,
+                                      const void* q, pa_dtype q_dtype, int num_seqs,
+                                      int num_q_heads, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* context_lens,
+                                      float sm_scale, int window, void* workspace,
+                                      size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  if (num_seqs > 0 && (!k_new || !v_new)) return PA_ERR_INVALID_ARG;
+  return decode_call(cache, out, q, q_dtype, num_seqs, num_q_heads, block_tables,
+                     max_blocks_per_seq, context_lens, sm_scale, window, 0, workspace,
+                     workspace_bytes, err_flag, stream, k_new, v_new, kv_dtype);
 }
 
 extern "C" pa_status pa_decode(const pa_cache* cache, void* out, const void* q, pa_dtype q_dtype,

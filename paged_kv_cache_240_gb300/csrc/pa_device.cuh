@@ -310,6 +310,46 @@ __device__ __forceinline__ float pow2i(int k) {  // 2^k for -126 <= k <= 127
   return __uint_as_float((uint32_t)(k + 127) << 23);
 }
 
+// ------------------------------------------------------------------ KV row write
+//
+// A new token's K or V row, one warp per row, E = D/32 consecutive elements per
+// lane: 16-bit inputs convert to fp32 exactly; the int8 quantiser finds amax by
+// a butterfly of shuffles (fmaxf/fabsf are exact) and rounds with the IEEE
+// operations __fdiv_rn and __float2int_rn, bit for bit the CPU oracle's rule.
+// The KV write kernel and the decode kernel that writes its step's token both
+// use these.
+template <typename IT>
+__device__ __forceinline__ float in_to_f32(IT x);
+template <>
+__device__ __forceinline__ float in_to_f32<__half>(__half x) {
+  return __half2float(x);
+}
+template <>
+__device__ __forceinline__ float in_to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+// Quantise one row held as E = D/32 consecutive elements per lane.
+template <int E>
+__device__ __forceinline__ void quantize_row(const float (&x)[E], uint8_t (&q)[E], float& scale) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int e = 0; e < E; e++) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  scale = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+  for (int e = 0; e < E; e++) {
+    int c = 0;
+    if (scale != 0.0f) {
+      c = __float2int_rn(__fdiv_rn(x[e], scale));
+      c = c > 127 ? 127 : (c < -127 ? -127 : c);
+    }
+    q[e] = (uint8_t)(c + 128);  // stored offset binary
+  }
+}
+
+
 // ------------------------------------------------------------------ dependent launch
 //
 // Programmatic dependent launch: a kernel launched with the programmatic

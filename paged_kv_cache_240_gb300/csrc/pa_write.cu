@@ -18,17 +18,6 @@
 
 namespace pa_dev {
 
-template <typename IT>
-__device__ __forceinline__ float in_to_f32(IT x);
-template <>
-__device__ __forceinline__ float in_to_f32<__half>(__half x) {
-  return __half2float(x);
-}
-template <>
-__device__ __forceinline__ float in_to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
-  return __bfloat162float(x);
-}
-
 struct WriteParams {
   const uint8_t* k;
   const uint8_t* v;
@@ -65,26 +54,6 @@ __global__ void __launch_bounds__(kWriteWarps * 32) write_copy_kernel(WriteParam
   const long long dst_row = ((long long)(slot / kBlock) * p.num_kv_heads + h) * kBlock + slot % kBlock;
   reinterpret_cast<V*>(p.k_cache + dst_row * kBytes)[lane] = kv;
   reinterpret_cast<V*>(p.v_cache + dst_row * kBytes)[lane] = vv;
-}
-
-// Quantise one row held as E = D/32 consecutive elements per lane.
-template <int E>
-__device__ __forceinline__ void quantize_row(const float (&x)[E], uint8_t (&q)[E], float& scale) {
-  float amax = 0.0f;
-#pragma unroll
-  for (int e = 0; e < E; e++) amax = fmaxf(amax, fabsf(x[e]));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  scale = __fdiv_rn(amax, 127.0f);
-#pragma unroll
-  for (int e = 0; e < E; e++) {
-    int c = 0;
-    if (scale != 0.0f) {
-      c = __float2int_rn(__fdiv_rn(x[e], scale));
-      c = c > 127 ? 127 : (c < -127 ? -127 : c);
-    }
-    q[e] = (uint8_t)(c + 128);  // stored offset binary
-  }
 }
 
 template <typename IT, int D>

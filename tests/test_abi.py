@@ -89,6 +89,23 @@ def test_decode_rejects_bad_arguments(lib):
     assert lib.pa_decode_workspace_bytes(2, 4, 2, 96, 4, 0, 0) == ctypes.c_size_t(-1).value
 
 
+def test_decode_append_rejects_bad_arguments(lib):
+    err = ctypes.c_void_p(16 * 99)
+
+    def call(c, **kw):
+        return lib.pa_decode_append(ctypes.byref(c), kw.get("k", 1280), kw.get("v", 1536),
+                                    kw.get("kvdt", 0), 256, 512, kw.get("qdt", 0),
+                                    kw.get("B", 2), kw.get("Hq", 4), 768, 4, 1024, 0.1, 0, None,
+                                    0, kw.get("err", err), None)
+    assert call(_cache(), Hq=3) == pa.PA_ERR_INVALID_ARG       # Hq % Hkv != 0
+    assert call(_cache(), qdt=1) == pa.PA_ERR_UNSUPPORTED      # q type != cache type
+    assert call(_cache(), k=None) == pa.PA_ERR_INVALID_ARG     # no new K rows
+    assert call(_cache(), v=1544) == pa.PA_ERR_INVALID_ARG     # misaligned new V rows
+    assert call(_cache(), kvdt=1) == pa.PA_ERR_UNSUPPORTED     # new rows' type != q's
+    assert call(_cache(), err=None) == pa.PA_ERR_INVALID_ARG
+    assert call(_cache(), B=0) == pa.PA_OK
+
+
 def test_prefill_rejects_bad_arguments(lib):
     err = ctypes.c_void_p(16 * 99)
 

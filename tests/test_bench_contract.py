@@ -53,6 +53,10 @@ class _Library:
         pass
 
     @staticmethod
+    def pa_decode_append(*args):
+        pass
+
+    @staticmethod
     def pa_prefill_chunk(*args):
         pass
 
@@ -97,7 +101,7 @@ def host_cuda(monkeypatch):
     import __graft_entry__
     import paged_kv_cache_240_gb300 as pa
     monkeypatch.setattr(__graft_entry__, "build", lambda: None)
-    for name in ("PagedCache", "pa_write_kv", "pa_decode", "pa_prefill_chunk",
+    for name in ("PagedCache", "pa_write_kv", "pa_decode", "pa_decode_append", "pa_prefill_chunk",
                  "pa_decode_workspace_bytes"):
         monkeypatch.setattr(pa, name, getattr(_Library, name))
 
@@ -127,7 +131,7 @@ def test_json_line(host_cuda, monkeypatch):
     assert line["config"]["workload"] == "qwen2.5-1.5b"
     assert abs(line["ms_per_step"] - STEP_MS) < 1e-12
     assert abs(line["value"] - w.kv_bytes() / (STEP_MS * 1e-3) / 1e9) < 1e-9
-    assert line["gpu_launches"] == 2 * steps  # the write and the decode, no reduce here
+    assert line["gpu_launches"] == steps  # one pa_decode_append launch, no merge kernel here
     r = line["roofline"]
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-12
