@@ -18,11 +18,15 @@ from gpu_util import (assert_close, bits_to_torch, cache_bits, i32, new_err, ora
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    ("tiny", dict(), None),
-    ("qwen2.5-1.5b", dict(num_seqs=8, lens=("uniform", 1, 1400)), None),   # cluster merge
-    ("qwen2.5-1.5b", dict(num_seqs=5, lens=("uniform", 1, 900)), 300),     # windowed
-    ("int8-kv", dict(num_seqs=6, lens=("uniform", 1, 700)), None),         # int8, workspace
-    ("mha-7b", dict(num_seqs=3, lens=("uniform", 17, 500)), None),
+    ("tiny", dict(), None, None),
+    ("qwen2.5-1.5b", dict(num_seqs=8, lens=("uniform", 1, 1400)), None, None),  # cluster merge
+    ("qwen2.5-1.5b", dict(num_seqs=5, lens=("uniform", 1, 900)), 300, None),    # windowed
+    ("int8-kv", dict(num_seqs=6, lens=("uniform", 1, 700)), None, None),        # int8, workspace
+    ("mha-7b", dict(num_seqs=3, lens=("uniform", 17, 500)), None, None),
+    # 16 query heads per kv head: two CTAs (row groups) hold each newest block and
+    # both write the same bytes into it
+    ("qwen2.5-1.5b", dict(num_seqs=4, lens=("uniform", 1, 900)), None, 16),
+    ("int8-kv", dict(num_seqs=3, lens=("uniform", 1, 500)), None, 16),
 ]
 
 
@@ -42,9 +46,11 @@ def _history(w):
             i32(slots[last]))
 
 
-@pytest.mark.parametrize("name,kw,window", CASES)
-def test_decode_append_matches_write_then_decode(name, kw, window, olib):
+@pytest.mark.parametrize("name,kw,window,G", CASES)
+def test_decode_append_matches_write_then_decode(name, kw, window, G, olib):
     w = I.make_workload(name, seed=77, window=window, **kw)
+    if G is not None:
+        w.num_kv_heads, w.num_q_heads = 2, 2 * G
     q_bits = I.query_rows(w)
     q = bits_to_torch(q_bits, w.q_dtype)
     tables, lens = i32(w.block_tables), i32(w.context_lens)
@@ -75,7 +81,7 @@ def test_decode_append_matches_write_then_decode(name, kw, window, olib):
     ref = oracle.attention(oc, q_bits, w.q_dtype, w.cu_q_lens, w.block_tables, w.context_lens,
                            sm_scale=sm, window=w.window, lib=olib)
     got = torch.from_numpy(outs[1]).view(q.dtype).double().numpy()
-    assert_close(got, ref, "pa_decode_append %s" % name)
+    assert_close(got, ref, "pa_decode_append %s G=%s" % (name, G))
 
 
 def test_decode_append_graph_replay_and_edge_rows():
