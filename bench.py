@@ -811,7 +811,9 @@ def measure(args, w, torch, pa, I, rank, world, steps, warmup, peaks, src):
     ms_per_step = total_ms / steps
     value = world * kv_step / (ms_per_step * 1e-3) / 1e9
     dec_ms, pre_ms = statistics.mean(r["dec_ms"]), statistics.mean(r["pre_ms"])
-    roof = roofline(w, dec_ms, pre_ms, peaks, src, full_size=args.num_seqs is None)
+    # recorded DRAM traffic belongs to the workload as defined: none for variants
+    roof = roofline(w, dec_ms, pre_ms, peaks, src,
+                    full_size=args.num_seqs is None and not getattr(args, "cache_dtype", None))
     cfg = workload_config(w)
     cfg["launch"] = "python calls" if args.no_graph else "CUDA graph replay of the step"
     if w.num_decode and w.num_decode < w.num_seqs:
@@ -886,6 +888,9 @@ def main():
                     help="int8-linear only: layers per step (default %d)" % LINEAR_LAYERS)
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="fewer decoding sequences (small profiling captures)")
+    ap.add_argument("--cache-dtype", choices=["f16", "bf16", "i8"], default=None,
+                    help="the workload's shapes over a cache of this type (a 16-bit cache "
+                         "takes queries of its own type; an int8 one keeps the workload's)")
     ap.add_argument("--extra-workloads", default="auto",
                     help="comma-separated workloads measured after the headline and reported "
                          "under 'workloads'; 'auto' = %s on one GPU with the default workload, "
@@ -899,6 +904,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     from paged_kv_cache_240_gb300 import inputs as I
     w = I.make_workload(args.workload, seed=args.seed, num_seqs=args.num_seqs)
+    if args.cache_dtype:
+        w.cache_dtype = args.cache_dtype
+        if args.cache_dtype != "i8":
+            w.q_dtype = args.cache_dtype
 
     if args.impl == "reference":
         if rank == 0:
